@@ -1,0 +1,17 @@
+"""fp64 CPU oracle for blockwise exact attention (test infrastructure only).
+
+Only the test suite, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` may import this package.  The CUDA product path never imports,
+links or calls it; the two share no code.
+"""
+from .attention import (  # noqa: F401
+    attention_fwd,
+    attention_probs,
+    attention_bwd,
+    attention_rows,
+    block_state,
+    merge_states,
+    finalize_state,
+    ring_fwd_blocked,
+    ring_schedule,
+)

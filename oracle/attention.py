@@ -1,0 +1,324 @@
+"""Plain fp64 CPU oracle for exact softmax attention, its gradients and the
+blockwise ring schedule.
+
+TEST INFRASTRUCTURE ONLY.  Nothing on the CUDA product path imports or calls
+this module; it shares no code, header, table or helper with it.  Inputs are
+the exact values handed to the GPU, upcast to float64.
+
+Sources (page title, section):
+
+* "Ring Attention: Train 1M Tokens on 8GB GPUs in 2026", section "Why Standard
+  Attention Explodes Past 100K Tokens": Attention(Q, K, V) =
+  softmax(Q K^T / sqrt(d_k)) V with Q, K, V in R^{N x d}.
+* same page, "Building Ring Attention in PyTorch: The 200-Line Version":
+  tensors laid out [seq, heads, head_dim]; scale = head_dim ** -0.5; the ring
+  loop visits one KV chunk per step; the output is divided by the softmax
+  denominator at the end.
+* same page, "Ring Attention: Partition Sequence Length, Not Batch": host i
+  owns rows [i N/P, (i+1) N/P); at every step each host passes its KV chunk to
+  host i+1 and takes host i-1's, P steps in all.
+* same page, "Gotchas and Failure Modes": partial results are carried as the
+  triple (max_score, exp_sum, weighted_output) and rescaled when merged.  The
+  printed sketch adds chunk results without the exp(m_chunk - m_new) factor;
+  its own text calls that a bug, so the oracle follows the rescaled triple
+  (online normaliser, Milakov & Gimelshein, cited on the arXiv 2310.01889 page
+  "Ring Attention with Blockwise Transformers for Near-Infinite Context").
+* "Ring Attention with Blockwise Transformers for Near-Infinite Context",
+  Abstract: the blockwise result is exact ("without resorting to
+  approximations"), so the plain definition is the reference and the blocked
+  mode below must agree with it to rounding.
+
+Readings where the pages are silent (each listed in the design notes):
+causal masking keeps key position <= query position (global positions,
+contiguous host blocks); grouped-query heads map query head h to key/value
+head h // (Hq / Hkv); a row that sees no key has m = -inf, l = 0, O = 0 and
+LSE = -inf; the backward pass differentiates L = sum(O * dO).
+
+Layout everywhere: [B, N, H, d] (the pages' [seq, heads, head_dim] plus a
+batch axis); LSE and the (m, l) state are [B, H, N].
+"""
+import numpy as np
+
+NEG_INF = -np.inf
+
+
+def _f64(x):
+    return np.asarray(x, dtype=np.float64)
+
+
+def _kv_head(h, hq, hkv):
+    """Query head h reads key/value head h // (Hq/Hkv) (grouped heads)."""
+    return h // (hq // hkv)
+
+
+def _visible(nq, nk, causal, q_off, kv_off):
+    """Boolean [nq, nk]: key j visible to query i (global positions)."""
+    if not causal:
+        return np.ones((nq, nk), dtype=bool)
+    qpos = q_off + np.arange(nq)[:, None]
+    kpos = kv_off + np.arange(nk)[None, :]
+    return kpos <= qpos
+
+
+def _scores(q2, k2, scale, vis):
+    """s_ij = scale * q_i . k_j on visible pairs, -inf elsewhere."""
+    s = scale * (q2 @ k2.T)
+    return np.where(vis, s, NEG_INF)
+
+
+def _row_lse(s):
+    """LSE_i = m_i + log sum_j exp(s_ij - m_i); -inf for an empty row."""
+    m = s.max(axis=1)
+    out = np.full(s.shape[0], NEG_INF)
+    ok = np.isfinite(m)
+    if ok.any():
+        e = np.exp(s[ok] - m[ok, None])
+        out[ok] = m[ok] + np.log(e.sum(axis=1))
+    return out
+
+
+def attention_probs(q, k, causal, scale, q_off=0, kv_off=0):
+    """Softmax matrix P [B, Hq, Nq, Nk] (small cases only).
+
+    Row i is exp(s_i - LSE_i); an empty row is all zeros.
+    """
+    q, k = _f64(q), _f64(k)
+    B, nq, hq, _ = q.shape
+    nk, hkv = k.shape[1], k.shape[2]
+    vis = _visible(nq, nk, causal, q_off, kv_off)
+    P = np.zeros((B, hq, nq, nk))
+    for b in range(B):
+        for h in range(hq):
+            s = _scores(q[b, :, h], k[b, :, _kv_head(h, hq, hkv)], scale, vis)
+            lse = _row_lse(s)
+            ok = np.isfinite(lse)
+            P[b, h, ok] = np.exp(s[ok] - lse[ok, None])
+    return P
+
+
+def attention_fwd(q, k, v, causal, scale, q_off=0, kv_off=0):
+    """Exact attention: O = softmax(scale Q K^T) V per (batch, head).
+
+    Returns (O [B, Nq, Hq, d], LSE [B, Hq, Nq]) in float64.
+    """
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    B, nq, hq, d = q.shape
+    nk, hkv = k.shape[1], k.shape[2]
+    vis = _visible(nq, nk, causal, q_off, kv_off)
+    O = np.zeros((B, nq, hq, d))
+    LSE = np.full((B, hq, nq), NEG_INF)
+    for b in range(B):
+        for h in range(hq):
+            g = _kv_head(h, hq, hkv)
+            s = _scores(q[b, :, h], k[b, :, g], scale, vis)
+            lse = _row_lse(s)
+            ok = np.isfinite(lse)
+            P = np.zeros_like(s)
+            P[ok] = np.exp(s[ok] - lse[ok, None])
+            O[b, :, h] = P @ v[b, :, g]
+            LSE[b, h] = lse
+    return O, LSE
+
+
+def attention_bwd(q, k, v, do, causal, scale):
+    """Gradients of L = sum(O * dO) for exact attention (self-attention, q_off = kv_off = 0).
+
+    P = exp(S - LSE); dV_j = sum_i P_ij dO_i; dP_ij = dO_i . v_j;
+    D_i = dO_i . O_i; dS_ij = P_ij (dP_ij - D_i); dQ_i = scale sum_j dS_ij k_j;
+    dK_j = scale sum_i dS_ij q_i.  Grouped heads sum dK, dV over the group.
+    Returns (dQ, dK, dV, O, LSE, D) in float64.
+    """
+    q, k, v, do = _f64(q), _f64(k), _f64(v), _f64(do)
+    B, n, hq, d = q.shape
+    hkv = k.shape[2]
+    vis = _visible(n, k.shape[1], causal, 0, 0)
+    dq = np.zeros_like(q)
+    dk = np.zeros_like(k)
+    dv = np.zeros_like(v)
+    O = np.zeros_like(q)
+    LSE = np.full((B, hq, n), NEG_INF)
+    Dd = np.zeros((B, hq, n))
+    for b in range(B):
+        for h in range(hq):
+            g = _kv_head(h, hq, hkv)
+            s = _scores(q[b, :, h], k[b, :, g], scale, vis)
+            lse = _row_lse(s)
+            ok = np.isfinite(lse)
+            P = np.zeros_like(s)
+            P[ok] = np.exp(s[ok] - lse[ok, None])
+            o = P @ v[b, :, g]
+            D = (do[b, :, h] * o).sum(axis=1)
+            dP = do[b, :, h] @ v[b, :, g].T
+            dS = P * (dP - D[:, None])
+            dq[b, :, h] = scale * (dS @ k[b, :, g])
+            dk[b, :, g] += scale * (dS.T @ q[b, :, h])
+            dv[b, :, g] += P.T @ do[b, :, h]
+            O[b, :, h] = o
+            LSE[b, h] = lse
+            Dd[b, h] = D
+    return dq, dk, dv, O, LSE, Dd
+
+
+def attention_rows(q, k, v, rows, causal, scale, do=None, want_kv_grads=False):
+    """Forward (and optionally backward) of selected query rows only.
+
+    ``rows`` is a sequence of (b, h, i).  Each row is computed from the plain
+    definition against every key it sees (no blocking).  Returns a dict with
+    O [R, d], LSE [R]; with ``do`` given also D [R] and dQ [R, d]; with
+    ``want_kv_grads`` also the contributions of exactly these rows to dK and
+    dV as dicts {(b, g): (dK [Nk, d], dV [Nk, d])}.  Under a causal mask the
+    last R query rows of every head of a group are the only rows that see the
+    last R keys, so their contributions are the complete dK, dV of those keys.
+
+    Rows of the same (b, h) are evaluated together through one matrix
+    product; rows remain independent.
+    """
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    if do is not None:
+        do = _f64(do)
+    B, n, hq, d = q.shape
+    nk, hkv = k.shape[1], k.shape[2]
+    rows = [tuple(int(x) for x in r) for r in rows]
+    R = len(rows)
+    out = {"O": np.zeros((R, d)), "LSE": np.full(R, NEG_INF)}
+    if do is not None:
+        out["D"] = np.zeros(R)
+        out["dQ"] = np.zeros((R, d))
+    kv_grads = {}
+    by_head = {}
+    for idx, (b, h, i) in enumerate(rows):
+        by_head.setdefault((b, h), []).append((idx, i))
+    for (b, h), items in by_head.items():
+        g = _kv_head(h, hq, hkv)
+        idxs = np.array([t[0] for t in items])
+        ii = np.array([t[1] for t in items])
+        kk, vv = k[b, :, g], v[b, :, g]
+        s = scale * (q[b, ii, h] @ kk.T)
+        if causal:
+            s = np.where(np.arange(nk)[None, :] <= ii[:, None], s, NEG_INF)
+        lse = _row_lse(s)
+        ok = np.isfinite(lse)
+        P = np.zeros_like(s)
+        P[ok] = np.exp(s[ok] - lse[ok, None])
+        o = P @ vv
+        out["O"][idxs] = o
+        out["LSE"][idxs] = lse
+        if do is None:
+            continue
+        dor = do[b, ii, h]
+        D = (dor * o).sum(axis=1)
+        dP = dor @ vv.T
+        dS = P * (dP - D[:, None])
+        out["D"][idxs] = D
+        out["dQ"][idxs] = scale * (dS @ kk)
+        if want_kv_grads:
+            dk_acc, dv_acc = kv_grads.setdefault(
+                (b, g), (np.zeros((nk, d)), np.zeros((nk, d))))
+            dk_acc += scale * (dS.T @ q[b, ii, h])
+            dv_acc += P.T @ dor
+    if want_kv_grads:
+        out["kv_grads"] = kv_grads
+    return out
+
+
+# ---------------------------------------------------------------------------
+# Blockwise mode: the ring schedule and the rescaled (max, exp_sum,
+# weighted_output) merge.  Used to pin the merge algebra against the plain
+# definition above, and as the reference for the block/merge entry points.
+# ---------------------------------------------------------------------------
+
+def ring_schedule(P, causal):
+    """Ring order of "Ring Attention: Partition Sequence Length, Not Batch":
+    at step s host i holds the KV chunk of host (i - s) mod P.  Returns, per
+    host, the list of chunks it computes against; under a causal mask chunks
+    wholly after the host's queries (j > i) are skipped."""
+    sched = []
+    for i in range(P):
+        blocks = [(i - s) % P for s in range(P)]
+        if causal:
+            blocks = [j for j in blocks if j <= i]
+        sched.append(blocks)
+    return sched
+
+
+def block_state(q, k, v, causal, scale, q_off, kv_off):
+    """Partial result of one (Q block, KV block) pair as the triple
+    (m [B,Hq,Nq], l [B,Hq,Nq], o [B,Nq,Hq,d]):
+    m_i = max_j s_ij, l_i = sum_j exp(s_ij - m_i), o_i = sum_j exp(s_ij - m_i) v_j.
+    A row with no visible key gives m = -inf, l = 0, o = 0."""
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    B, nq, hq, d = q.shape
+    nk, hkv = k.shape[1], k.shape[2]
+    vis = _visible(nq, nk, causal, q_off, kv_off)
+    m = np.full((B, hq, nq), NEG_INF)
+    l = np.zeros((B, hq, nq))
+    o = np.zeros((B, nq, hq, d))
+    for b in range(B):
+        for h in range(hq):
+            g = _kv_head(h, hq, hkv)
+            s = _scores(q[b, :, h], k[b, :, g], scale, vis)
+            mm = s.max(axis=1)
+            ok = np.isfinite(mm)
+            e = np.zeros_like(s)
+            e[ok] = np.exp(s[ok] - mm[ok, None])
+            m[b, h] = mm
+            l[b, h] = e.sum(axis=1)
+            o[b, :, h] = e @ v[b, :, g]
+    return m, l, o
+
+
+def merge_states(a, b):
+    """Merge two triples: m = max(m_a, m_b); each side is rescaled by
+    exp(m_side - m) before summing l and o.  A side with m = -inf (nothing
+    seen) gets weight 0."""
+    ma, la, oa = (_f64(x) for x in a)
+    mb, lb, ob = (_f64(x) for x in b)
+    m = np.maximum(ma, mb)
+    fin = np.isfinite(m)
+    wa = np.zeros_like(m)
+    wb = np.zeros_like(m)
+    wa[fin] = np.where(np.isfinite(ma[fin]), np.exp(ma[fin] - m[fin]), 0.0)
+    wb[fin] = np.where(np.isfinite(mb[fin]), np.exp(mb[fin] - m[fin]), 0.0)
+    l = wa * la + wb * lb
+    # weights are [B, H, N]; o is [B, N, H, d]
+    wa_o = np.transpose(wa, (0, 2, 1))[..., None]
+    wb_o = np.transpose(wb, (0, 2, 1))[..., None]
+    o = wa_o * oa + wb_o * ob
+    return m, l, o
+
+
+def finalize_state(state):
+    """O = o / l and LSE = m + log l; a row with l = 0 gives O = 0, LSE = -inf."""
+    m, l, o = (_f64(x) for x in state)
+    ok = l > 0
+    LSE = np.full_like(m, NEG_INF)
+    LSE[ok] = m[ok] + np.log(l[ok])
+    inv = np.zeros_like(l)
+    inv[ok] = 1.0 / l[ok]
+    O = o * np.transpose(inv, (0, 2, 1))[..., None]
+    return O, LSE
+
+
+def ring_fwd_blocked(q, k, v, P, causal, scale):
+    """Forward pass as the ring computes it: host i starts from the empty
+    triple and, in ring order, merges the partial result of its queries
+    against each KV chunk it holds; finally divides by the denominator."""
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    B, n, hq, d = q.shape
+    if n % P:
+        raise ValueError("P must divide N")
+    S = n // P
+    O = np.zeros((B, n, hq, d))
+    LSE = np.full((B, hq, n), NEG_INF)
+    for i, blocks in enumerate(ring_schedule(P, causal)):
+        qi = q[:, i * S:(i + 1) * S]
+        acc = (np.full((B, hq, S), NEG_INF), np.zeros((B, hq, S)),
+               np.zeros((B, S, hq, d)))
+        for j in blocks:
+            part = block_state(qi, k[:, j * S:(j + 1) * S], v[:, j * S:(j + 1) * S],
+                               causal, scale, i * S, j * S)
+            acc = merge_states(acc, part)
+        Oi, Li = finalize_state(acc)
+        O[:, i * S:(i + 1) * S] = Oi
+        LSE[:, :, i * S:(i + 1) * S] = Li
+    return O, LSE
