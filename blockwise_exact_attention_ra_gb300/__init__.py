@@ -1,0 +1,242 @@
+"""Python binding of libra (blockwise exact attention, ring-emulated, sm_103a).
+
+Argument marshalling only: every step of the computation runs in the CUDA
+kernels behind the C ABI declared in include/ra.h.  PyTorch supplies device
+memory and streams.  Importing this package without the compiled library
+raises ImportError; there is no other implementation to fall back to.
+
+Functions with the C names (``ra_block_fwd``, ``ra_merge``, ``ra_ring_fwd``,
+``ra_ring_bwd``, ...) take torch tensors in the [B, N, H, d] layout and raise
+``RAError`` on a non-OK status.  ``ring_attention_fwd`` / ``ring_attention_bwd``
+additionally allocate outputs and workspace with torch.
+"""
+import ctypes
+import os
+
+import torch
+
+__all__ = [
+    "RAError", "RaShape", "lib", "shape_of",
+    "ra_acc_init", "ra_block_fwd", "ra_block_fwd_workspace_bytes", "ra_merge", "ra_finalize",
+    "ra_ring_fwd", "ra_ring_fwd_workspace_bytes", "ra_ring_bwd", "ra_ring_bwd_workspace_bytes",
+    "ra_sync_status", "ra_last_error", "ra_launch_count", "ra_selftest_timeout",
+    "ra_kernel_timing", "ra_kernel_timing_read",
+    "ring_attention_fwd", "ring_attention_bwd", "RA_F32", "RA_BF16", "RA_F16",
+]
+
+RA_F32, RA_BF16, RA_F16 = 0, 1, 2
+STATUS = {0: "RA_OK", 1: "RA_ERR_INVALID_ARG", 2: "RA_ERR_UNSUPPORTED", 3: "RA_ERR_CUDA",
+          4: "RA_ERR_RANGE", 5: "RA_ERR_TIMEOUT"}
+_DTYPES = {torch.float32: RA_F32, torch.bfloat16: RA_BF16, torch.float16: RA_F16}
+_TORCH = {v: k for k, v in _DTYPES.items()}
+
+_LIBPATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libra.so")
+
+
+class RAError(RuntimeError):
+    def __init__(self, code, msg):
+        super().__init__(f"{STATUS.get(code, code)}: {msg}")
+        self.code = code
+
+
+class RaShape(ctypes.Structure):
+    _fields_ = [("B", ctypes.c_int), ("N_q", ctypes.c_int), ("N_kv", ctypes.c_int),
+                ("Hq", ctypes.c_int), ("Hkv", ctypes.c_int), ("d", ctypes.c_int),
+                ("q_bstride", ctypes.c_longlong), ("kv_bstride", ctypes.c_longlong)]
+
+
+def _load():
+    if not os.path.exists(_LIBPATH):
+        raise ImportError(
+            f"{_LIBPATH} is missing: build it with `python -c 'import __graft_entry__ as g; g.build()'` "
+            "(or python blockwise_exact_attention_ra_gb300/build.py)")
+    L = ctypes.CDLL(_LIBPATH)
+    vp, i, f, ll, sz, sh = (ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_longlong,
+                            ctypes.c_size_t, RaShape)
+    sig = {
+        "ra_acc_init": (i, [vp, vp, vp, sh, vp]),
+        "ra_block_fwd": (i, [vp, vp, vp, i, vp, vp, vp, sh, ll, ll, i, f, vp, sz, vp]),
+        "ra_block_fwd_workspace_bytes": (sz, [i, sh]),
+        "ra_merge": (i, [vp, vp, vp, vp, vp, vp, sh, vp]),
+        "ra_finalize": (i, [vp, vp, vp, vp, i, vp, sh, vp]),
+        "ra_ring_fwd": (i, [vp, vp, vp, i, sh, i, i, f, vp, i, vp, vp, sz, vp]),
+        "ra_ring_fwd_workspace_bytes": (sz, [i, sh, i]),
+        "ra_ring_bwd": (i, [vp, vp, vp, vp, i, vp, vp, i, sh, i, i, f, vp, vp, vp, i, vp, sz, vp]),
+        "ra_ring_bwd_workspace_bytes": (sz, [i, i, sh, i]),
+        "ra_sync_status": (i, [vp]),
+        "ra_last_error": (ctypes.c_char_p, []),
+        "ra_launch_count": (ctypes.c_ulonglong, []),
+        "ra_selftest_timeout": (i, [ctypes.c_uint, vp]),
+        "ra_kernel_timing": (i, [i]),
+        "ra_kernel_timing_read": (i, [i, ctypes.POINTER(ctypes.c_double),
+                                      ctypes.POINTER(ctypes.c_ulonglong)]),
+    }
+    for name, (res, args) in sig.items():
+        fn = getattr(L, name)
+        fn.restype = res
+        fn.argtypes = args
+    return L
+
+
+lib = _load()
+
+
+def ra_last_error():
+    return lib.ra_last_error().decode()
+
+
+def ra_launch_count():
+    return int(lib.ra_launch_count())
+
+
+def _check(code):
+    if code != 0:
+        raise RAError(code, ra_last_error())
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _dt(t):
+    try:
+        return _DTYPES[t.dtype]
+    except KeyError:
+        raise RAError(1, f"unsupported dtype {t.dtype}") from None
+
+
+def _bstride(t):
+    return t.stride(0)
+
+
+def _check_layout(t, name):
+    """Tensors are [B, N, H, d] with rows of H*d contiguous elements."""
+    if t.dim() != 4:
+        raise RAError(1, f"{name} must be [B, N, H, d]")
+    B, N, H, d = t.shape
+    if t.stride(3) != 1 or t.stride(2) != d or t.stride(1) != H * d:
+        raise RAError(1, f"{name} must have contiguous [N, H, d] rows (strides {t.stride()})")
+
+
+def shape_of(q, k):
+    """RaShape for q [B, Nq, Hq, d] and k [B, Nkv, Hkv, d] (batch strides taken
+    from the tensors)."""
+    _check_layout(q, "q")
+    _check_layout(k, "k")
+    B, Nq, Hq, d = q.shape
+    _, Nkv, Hkv, _ = k.shape
+    return RaShape(B, Nq, Nkv, Hq, Hkv, d, _bstride(q), _bstride(k))
+
+
+RA_KERNEL_FWD_TC, RA_KERNEL_BWD_TC, RA_KERNEL_FWD_F32, RA_KERNEL_BWD_F32 = 0, 1, 2, 3
+
+
+def ra_kernel_timing(enable):
+    _check(lib.ra_kernel_timing(int(bool(enable))))
+
+
+def ra_kernel_timing_read(kernel):
+    """(total device ms, launches) of one kernel since timing was enabled."""
+    ms = ctypes.c_double()
+    n = ctypes.c_ulonglong()
+    _check(lib.ra_kernel_timing_read(int(kernel), ctypes.byref(ms), ctypes.byref(n)))
+    return ms.value, int(n.value)
+
+
+def ra_sync_status(stream=None):
+    _check(lib.ra_sync_status(_stream(stream)))
+
+
+def ra_selftest_timeout(timeout_us, stream=None):
+    _check(lib.ra_selftest_timeout(int(timeout_us), _stream(stream)))
+
+
+def ra_acc_init(o_acc, m_acc, l_acc, shape, stream=None):
+    _check(lib.ra_acc_init(_ptr(o_acc), _ptr(m_acc), _ptr(l_acc), shape, _stream(stream)))
+
+
+def ra_block_fwd_workspace_bytes(dtype, shape):
+    return int(lib.ra_block_fwd_workspace_bytes(dtype, shape))
+
+
+def ra_block_fwd(q, k_blk, v_blk, o_acc, m_acc, l_acc, q_off, kv_off, causal, scale,
+                 workspace=None, shape=None, stream=None):
+    """Fold one key/value block into the running state of a query block."""
+    shape = shape or shape_of(q, k_blk)
+    dt = _dt(q)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(lib.ra_block_fwd(_ptr(q), _ptr(k_blk), _ptr(v_blk), dt, _ptr(o_acc), _ptr(m_acc),
+                            _ptr(l_acc), shape, int(q_off), int(kv_off), int(bool(causal)),
+                            float(scale), _ptr(workspace), ws_bytes, _stream(stream)))
+
+
+def ra_merge(o_a, m_a, l_a, o_b, m_b, l_b, shape, stream=None):
+    _check(lib.ra_merge(_ptr(o_a), _ptr(m_a), _ptr(l_a), _ptr(o_b), _ptr(m_b), _ptr(l_b),
+                        shape, _stream(stream)))
+
+
+def ra_finalize(o_acc, m_acc, l_acc, o_out, lse, shape, stream=None):
+    _check(lib.ra_finalize(_ptr(o_acc), _ptr(m_acc), _ptr(l_acc), _ptr(o_out), _dt(o_out),
+                           _ptr(lse), shape, _stream(stream)))
+
+
+def ra_ring_fwd_workspace_bytes(dtype, shape, P):
+    return int(lib.ra_ring_fwd_workspace_bytes(dtype, shape, P))
+
+
+def ra_ring_fwd(q, k, v, P, causal, scale, o, lse, workspace=None, stream=None):
+    shape = shape_of(q, k)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(lib.ra_ring_fwd(_ptr(q), _ptr(k), _ptr(v), _dt(q), shape, int(P), int(bool(causal)),
+                           float(scale), _ptr(o), _dt(o), _ptr(lse), _ptr(workspace), ws_bytes,
+                           _stream(stream)))
+
+
+def ra_ring_bwd_workspace_bytes(dtype, grad_dtype, shape, P):
+    return int(lib.ra_ring_bwd_workspace_bytes(dtype, grad_dtype, shape, P))
+
+
+def ra_ring_bwd(q, k, v, o, dO, lse, P, causal, scale, dq, dk, dv, workspace, stream=None):
+    shape = shape_of(q, k)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(lib.ra_ring_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _dt(o), _ptr(dO), _ptr(lse),
+                           _dt(q), shape, int(P), int(bool(causal)), float(scale), _ptr(dq),
+                           _ptr(dk), _ptr(dv), _dt(dq), _ptr(workspace), ws_bytes,
+                           _stream(stream)))
+
+
+def _workspace(nbytes, device):
+    return torch.empty(max(int(nbytes), 16), dtype=torch.uint8, device=device)
+
+
+def ring_attention_fwd(q, k, v, P, causal=True, scale=None, o_dtype=torch.float32,
+                       stream=None):
+    """Allocate O [B,N,Hq,d] (o_dtype) and LSE [B,Hq,N] fp32 and run the ring forward."""
+    if scale is None:
+        scale = q.shape[-1] ** -0.5
+    B, N, Hq, d = q.shape
+    o = torch.empty(B, N, Hq, d, dtype=o_dtype, device=q.device)
+    lse = torch.empty(B, Hq, N, dtype=torch.float32, device=q.device)
+    ws = _workspace(ra_ring_fwd_workspace_bytes(_dt(q), shape_of(q, k), P), q.device)
+    ra_ring_fwd(q, k, v, P, causal, scale, o, lse, ws, stream)
+    return o, lse
+
+
+def ring_attention_bwd(q, k, v, o, lse, dO, P, causal=True, scale=None,
+                       grad_dtype=torch.float32, stream=None):
+    """Allocate dQ, dK, dV (grad_dtype) and workspace and run the ring backward."""
+    if scale is None:
+        scale = q.shape[-1] ** -0.5
+    dq = torch.empty(q.shape, dtype=grad_dtype, device=q.device)
+    dk = torch.empty(k.shape, dtype=grad_dtype, device=q.device)
+    dv = torch.empty(v.shape, dtype=grad_dtype, device=q.device)
+    ws = _workspace(ra_ring_bwd_workspace_bytes(_dt(q), _DTYPES[grad_dtype], shape_of(q, k), P),
+                    q.device)
+    ra_ring_bwd(q, k, v, o, dO, lse, P, causal, scale, dq, dk, dv, ws, stream)
+    return dq, dk, dv

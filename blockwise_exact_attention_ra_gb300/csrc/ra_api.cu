@@ -1,0 +1,642 @@
+// C-ABI front end of libra: argument validation, workspace layout, tensor
+// map encoding and kernel dispatch.  Every entry point only enqueues work on
+// the caller's stream; nothing here allocates device memory.
+#include <math.h>
+#include <stdarg.h>
+#include <stdio.h>
+#include <stdlib.h>
+#include <string.h>
+
+#include <atomic>
+#include <mutex>
+#include <string>
+#include <utility>
+#include <vector>
+
+#include "ra_internal.h"
+
+// One status word per device (module-global storage, not an allocation).
+__device__ int g_ra_status_word;
+
+namespace ra {
+
+static std::atomic<unsigned long long> g_launches{0};
+void count_launch(unsigned n) { g_launches.fetch_add(n, std::memory_order_relaxed); }
+
+namespace {
+
+thread_local std::string t_err;
+
+int fail(int code, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  t_err = buf;
+  return code;
+}
+
+int cuda_fail(cudaError_t e, const char* what) {
+  return fail(RA_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceCache {
+  std::mutex mu;
+  int* status[kMaxDevices] = {};
+  int sms[kMaxDevices] = {};
+  int cc_major[kMaxDevices] = {};
+  int cc_minor[kMaxDevices] = {};
+};
+DeviceCache& cache() {
+  static DeviceCache c;
+  return c;
+}
+
+int current_device(int* dev) {
+  cudaError_t e = cudaGetDevice(dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (*dev < 0 || *dev >= kMaxDevices) return fail(RA_ERR_UNSUPPORTED, "device ordinal %d", *dev);
+  return RA_OK;
+}
+
+// Address of this device's status word, looked up once per device.
+int status_ptr(int** out) {
+  int dev;
+  int rc = current_device(&dev);
+  if (rc) return rc;
+  DeviceCache& c = cache();
+  std::lock_guard<std::mutex> lk(c.mu);
+  if (!c.status[dev]) {
+    void* p = nullptr;
+    cudaError_t e = cudaGetSymbolAddress(&p, g_ra_status_word);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(status word)");
+    c.status[dev] = static_cast<int*>(p);
+    cudaDeviceGetAttribute(&c.sms[dev], cudaDevAttrMultiProcessorCount, dev);
+    cudaDeviceGetAttribute(&c.cc_major[dev], cudaDevAttrComputeCapabilityMajor, dev);
+    cudaDeviceGetAttribute(&c.cc_minor[dev], cudaDevAttrComputeCapabilityMinor, dev);
+  }
+  *out = c.status[dev];
+  return RA_OK;
+}
+
+int device_sms() {
+  int dev = 0;
+  cudaGetDevice(&dev);
+  return cache().sms[dev] > 0 ? cache().sms[dev] : 1;
+}
+
+bool device_is_sm103() {
+  int dev = 0;
+  cudaGetDevice(&dev);
+  return cache().cc_major[dev] == 10 && cache().cc_minor[dev] == 3;
+}
+
+unsigned long long wait_limit_ns() {
+  static unsigned long long v = [] {
+    const char* s = getenv("RA_WAIT_TIMEOUT_MS");
+    unsigned long long ms = s ? strtoull(s, nullptr, 10) : 10000ull;
+    if (ms == 0) ms = 10000ull;
+    return ms * 1000000ull;
+  }();
+  return v;
+}
+
+// -------------------------------------------------------------- tensor maps
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion,
+                                  CUtensorMapFloatOOBfill);
+
+int encoder(EncodeTiledFn* fn) {
+  static EncodeTiledFn f = nullptr;
+  static std::once_flag once;
+  static cudaError_t err = cudaSuccess;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    err = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                           &q);
+    if (err == cudaSuccess && q == cudaDriverEntryPointSuccess) f = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  if (!f) return fail(RA_ERR_CUDA, "cuTensorMapEncodeTiled unavailable (%s)", cudaGetErrorString(err));
+  *fn = f;
+  return RA_OK;
+}
+
+// [B, N, H, d] 16-bit tensor, batch stride bs (elements): dims (d, H, N, B),
+// box (64, 1, 128, 1), 128-byte swizzle; rows past N read as zeros.
+int make_map(CUtensorMap* m, const void* base, int is_bf16, int B, int N, int H, int d,
+             long long bs) {
+  EncodeTiledFn fn;
+  int rc = encoder(&fn);
+  if (rc) return rc;
+  cuuint64_t dims[4] = {(cuuint64_t)d, (cuuint64_t)H, (cuuint64_t)N, (cuuint64_t)B};
+  cuuint64_t strides[3] = {(cuuint64_t)d * 2, (cuuint64_t)H * d * 2, (cuuint64_t)bs * 2};
+  cuuint32_t box[4] = {64, 1, 128, 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = fn(m, is_bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4,
+                  const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(RA_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+  return RA_OK;
+}
+
+// -------------------------------------------------------------- validation
+size_t dtype_size(int dt) { return dt == RA_F32 ? 4 : 2; }
+bool valid_dtype(int dt) { return dt == RA_F32 || dt == RA_BF16 || dt == RA_F16; }
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+struct Shape {
+  int B, Nq, Nkv, Hq, Hkv, d;
+  long long q_bs, kv_bs;
+};
+
+int check_shape(const ra_shape& s, Shape* out) {
+  if (s.B < 1 || s.N_q < 1 || s.N_kv < 1 || s.Hq < 1 || s.Hkv < 1 || s.d < 1)
+    return fail(RA_ERR_INVALID_ARG, "shape has a non-positive extent (B=%d N_q=%d N_kv=%d Hq=%d Hkv=%d d=%d)",
+                s.B, s.N_q, s.N_kv, s.Hq, s.Hkv, s.d);
+  if (s.Hq % s.Hkv) return fail(RA_ERR_INVALID_ARG, "Hq=%d is not a multiple of Hkv=%d", s.Hq, s.Hkv);
+  if (s.N_q >= (1 << 30) || s.N_kv >= (1 << 30) || s.Hq > 4096 || s.d > 4096)
+    return fail(RA_ERR_INVALID_ARG, "shape extent too large");
+  Shape r{s.B, s.N_q, s.N_kv, s.Hq, s.Hkv, s.d, s.q_bstride, s.kv_bstride};
+  const long long qrow = (long long)s.N_q * s.Hq * s.d, kvrow = (long long)s.N_kv * s.Hkv * s.d;
+  if (r.q_bs == 0) r.q_bs = qrow;
+  if (r.kv_bs == 0) r.kv_bs = kvrow;
+  if (r.q_bs < qrow || r.kv_bs < kvrow)
+    return fail(RA_ERR_INVALID_ARG, "batch stride smaller than one batch (q %lld < %lld or kv %lld < %lld)",
+                r.q_bs, qrow, r.kv_bs, kvrow);
+  *out = r;
+  return RA_OK;
+}
+
+int check_ptr(const void* p, const char* name) {
+  if (!p) return fail(RA_ERR_INVALID_ARG, "%s is NULL", name);
+  if (!aligned16(p)) return fail(RA_ERR_INVALID_ARG, "%s is not 16-byte aligned", name);
+  return RA_OK;
+}
+
+int check_scale(float scale) {
+  if (!(scale > 0.f) || !isfinite(scale))
+    return fail(RA_ERR_INVALID_ARG, "scale must be finite and > 0 (got %g)", (double)scale);
+  return RA_OK;
+}
+
+// Tensor-core path prerequisites (d, strides, device).
+int check_tc(const Shape& s, int dtype) {
+  if (s.d != 64 && s.d != 128)
+    return fail(RA_ERR_UNSUPPORTED, "tensor-core path supports d in {64, 128} (got %d)", s.d);
+  if (((s.q_bs * 2) & 15) || ((s.kv_bs * 2) & 15))
+    return fail(RA_ERR_INVALID_ARG, "batch strides must be multiples of 16 bytes");
+  if (!device_is_sm103())
+    return fail(RA_ERR_UNSUPPORTED, "tensor-core kernels are built for sm_103a only");
+  (void)dtype;
+  return RA_OK;
+}
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+// ------------------------------------------------------------ kernel timing
+struct KernelTimer {
+  std::mutex mu;
+  bool on = false;
+  std::vector<std::pair<cudaEvent_t, cudaEvent_t>> ev[RA_KERNEL_COUNT];
+};
+KernelTimer& ktimer() {
+  static KernelTimer t;
+  return t;
+}
+void ktimer_clear(KernelTimer& t) {
+  for (auto& v : t.ev) {
+    for (auto& p : v) {
+      cudaEventDestroy(p.first);
+      cudaEventDestroy(p.second);
+    }
+    v.clear();
+  }
+}
+
+// Brackets one launch with events when timing is on.
+struct TimedLaunch {
+  int id;
+  cudaStream_t st;
+  cudaEvent_t a = nullptr, b = nullptr;
+  TimedLaunch(int kid, cudaStream_t s) : id(kid), st(s) {
+    KernelTimer& t = ktimer();
+    std::lock_guard<std::mutex> lk(t.mu);
+    if (!t.on) return;
+    if (cudaEventCreate(&a) != cudaSuccess || cudaEventCreate(&b) != cudaSuccess) {
+      a = b = nullptr;
+      return;
+    }
+    cudaEventRecord(a, st);
+  }
+  ~TimedLaunch() {
+    if (!a) return;
+    cudaEventRecord(b, st);
+    KernelTimer& t = ktimer();
+    std::lock_guard<std::mutex> lk(t.mu);
+    t.ev[id].emplace_back(a, b);
+  }
+};
+
+}  // namespace
+}  // namespace ra
+
+using namespace ra;
+
+extern "C" {
+#pragma GCC visibility push(default)
+
+const char* ra_last_error(void) { return t_err.c_str(); }
+
+unsigned long long ra_launch_count(void) { return g_launches.load(); }
+
+int ra_kernel_timing(int enable) {
+  KernelTimer& t = ktimer();
+  std::lock_guard<std::mutex> lk(t.mu);
+  ktimer_clear(t);
+  t.on = enable != 0;
+  return RA_OK;
+}
+
+int ra_kernel_timing_read(int kernel, double* total_ms, unsigned long long* launches) {
+  if (kernel < 0 || kernel >= RA_KERNEL_COUNT || !total_ms || !launches)
+    return fail(RA_ERR_INVALID_ARG, "bad kernel id or NULL output");
+  KernelTimer& t = ktimer();
+  std::lock_guard<std::mutex> lk(t.mu);
+  double sum = 0.0;
+  for (auto& p : t.ev[kernel]) {
+    cudaError_t e = cudaEventSynchronize(p.second);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaEventSynchronize");
+    float ms = 0.f;
+    e = cudaEventElapsedTime(&ms, p.first, p.second);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaEventElapsedTime");
+    sum += ms;
+  }
+  *total_ms = sum;
+  *launches = t.ev[kernel].size();
+  return RA_OK;
+}
+
+int ra_sync_status(void* stream) {
+  int* st;
+  int rc = status_ptr(&st);
+  if (rc) return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+  int v = 0;
+  e = cudaMemcpyFromSymbol(&v, g_ra_status_word, sizeof v);
+  if (e != cudaSuccess) return cuda_fail(e, "read status word");
+  if (v) {
+    const int zero = 0;
+    e = cudaMemcpyToSymbol(g_ra_status_word, &zero, sizeof zero);
+    if (e != cudaSuccess) return cuda_fail(e, "clear status word");
+    return fail(v, v == RA_ERR_RANGE ? "an operand exceeded the fp16 range"
+                                     : v == RA_ERR_TIMEOUT ? "a bounded wait on the device gave up"
+                                                           : "device reported status %d",
+                v);
+  }
+  t_err.clear();
+  return RA_OK;
+}
+
+int ra_selftest_timeout(unsigned int timeout_us, void* stream) {
+  int* st;
+  int rc = status_ptr(&st);
+  if (rc) return rc;
+  if (timeout_us == 0 || timeout_us > 10000000u)
+    return fail(RA_ERR_INVALID_ARG, "timeout_us must be in (0, 1e7]");
+  cudaError_t e = launch_selftest_timeout(timeout_us, st, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? RA_OK : cuda_fail(e, "selftest_timeout launch");
+}
+
+int ra_acc_init(float* o_acc, float* m_acc, float* l_acc, ra_shape shape, void* stream) {
+  Shape s;
+  int rc;
+  if ((rc = check_shape(shape, &s))) return rc;
+  if ((rc = check_ptr(o_acc, "o_acc")) || (rc = check_ptr(m_acc, "m_acc")) || (rc = check_ptr(l_acc, "l_acc")))
+    return rc;
+  int* st;
+  if ((rc = status_ptr(&st))) return rc;
+  cudaError_t e = launch_acc_init(o_acc, m_acc, l_acc, s.B, s.Nq, s.Hq, s.d,
+                                  static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? RA_OK : cuda_fail(e, "acc_init launch");
+}
+
+int ra_merge(float* o_a, float* m_a, float* l_a, const float* o_b, const float* m_b,
+             const float* l_b, ra_shape shape, void* stream) {
+  Shape s;
+  int rc;
+  if ((rc = check_shape(shape, &s))) return rc;
+  if ((rc = check_ptr(o_a, "o_a")) || (rc = check_ptr(m_a, "m_a")) || (rc = check_ptr(l_a, "l_a")) ||
+      (rc = check_ptr(o_b, "o_b")) || (rc = check_ptr(m_b, "m_b")) || (rc = check_ptr(l_b, "l_b")))
+    return rc;
+  int* st;
+  if ((rc = status_ptr(&st))) return rc;
+  cudaError_t e = launch_merge(o_a, m_a, l_a, o_b, m_b, l_b, s.B, s.Nq, s.Hq, s.d,
+                               static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? RA_OK : cuda_fail(e, "merge launch");
+}
+
+int ra_finalize(const float* o_acc, const float* m_acc, const float* l_acc, void* o_out,
+                ra_dtype o_dtype, float* lse, ra_shape shape, void* stream) {
+  Shape s;
+  int rc;
+  if ((rc = check_shape(shape, &s))) return rc;
+  if (!valid_dtype(o_dtype)) return fail(RA_ERR_INVALID_ARG, "bad o_dtype %d", (int)o_dtype);
+  if ((rc = check_ptr(o_acc, "o_acc")) || (rc = check_ptr(m_acc, "m_acc")) || (rc = check_ptr(l_acc, "l_acc")) ||
+      (rc = check_ptr(o_out, "o_out")) || (rc = check_ptr(lse, "lse")))
+    return rc;
+  int* st;
+  if ((rc = status_ptr(&st))) return rc;
+  cudaError_t e = launch_finalize(o_acc, m_acc, l_acc, o_out, o_dtype, s.q_bs, lse, s.B, s.Nq,
+                                  s.Hq, s.d, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? RA_OK : cuda_fail(e, "finalize launch");
+}
+
+size_t ra_block_fwd_workspace_bytes(ra_dtype dtype, ra_shape shape) {
+  if (dtype != RA_BF16 || shape.B < 1 || shape.N_kv < 1 || shape.Hkv < 1 || shape.d < 1) return 0;
+  return align256((size_t)shape.B * shape.N_kv * shape.Hkv * shape.d * 2);
+}
+
+int ra_block_fwd(const void* q, const void* k_blk, const void* v_blk, ra_dtype dtype,
+                 float* o_acc, float* m_acc, float* l_acc, ra_shape shape, long long q_off,
+                 long long kv_off, int causal, float scale, void* workspace, size_t ws_bytes,
+                 void* stream) {
+  Shape s;
+  int rc;
+  if ((rc = check_shape(shape, &s))) return rc;
+  if (!valid_dtype(dtype)) return fail(RA_ERR_INVALID_ARG, "bad dtype %d", (int)dtype);
+  if ((rc = check_scale(scale))) return rc;
+  if ((rc = check_ptr(q, "q")) || (rc = check_ptr(k_blk, "k_blk")) || (rc = check_ptr(v_blk, "v_blk")) ||
+      (rc = check_ptr(o_acc, "o_acc")) || (rc = check_ptr(m_acc, "m_acc")) || (rc = check_ptr(l_acc, "l_acc")))
+    return rc;
+  if (q_off < 0 || kv_off < 0) return fail(RA_ERR_INVALID_ARG, "offsets must be >= 0");
+  int* st;
+  if ((rc = status_ptr(&st))) return rc;
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  if (dtype == RA_F32) {
+    if (s.d != 32 && s.d != 64 && s.d != 128)
+      return fail(RA_ERR_UNSUPPORTED, "fp32 path supports d in {32, 64, 128} (got %d)", s.d);
+    SimtFwdArgs a{};
+    a.q = static_cast<const float*>(q);
+    a.k = static_cast<const float*>(k_blk);
+    a.v = static_cast<const float*>(v_blk);
+    a.B = s.B; a.Nq = s.Nq; a.Nkv = s.Nkv; a.Hq = s.Hq; a.Hkv = s.Hkv; a.d = s.d;
+    a.q_bs = s.q_bs; a.kv_bs = s.kv_bs;
+    a.scale = scale; a.causal = causal != 0; a.q_off = q_off; a.kv_off = kv_off;
+    a.P = 0; a.S = 0;
+    a.o_acc = o_acc; a.m_acc = m_acc; a.l_acc = l_acc;
+    TimedLaunch tl(RA_KERNEL_FWD_F32, cs);
+    cudaError_t e = launch_simt_fwd(a, cs);
+    return e == cudaSuccess ? RA_OK : cuda_fail(e, "fp32 block forward launch");
+  }
+  if ((rc = check_tc(s, dtype))) return rc;
+  const void* v16 = v_blk;
+  if (dtype == RA_BF16) {
+    const size_t need = ra_block_fwd_workspace_bytes(dtype, shape);
+    if (!workspace || ws_bytes < need)
+      return fail(RA_ERR_INVALID_ARG, "workspace of %zu bytes needed (got %zu)", need, ws_bytes);
+    if ((rc = check_ptr(workspace, "workspace"))) return rc;
+    cudaError_t e = launch_to_f16(v_blk, RA_BF16, s.kv_bs, workspace, s.B,
+                                  (long long)s.Nkv * s.Hkv * s.d, st, cs);
+    if (e != cudaSuccess) return cuda_fail(e, "v -> fp16 launch");
+    v16 = workspace;
+  }
+  TcFwdArgs a;
+  memset(&a, 0, sizeof a);
+  const int bf = dtype == RA_BF16;
+  if ((rc = make_map(&a.tm_q, q, bf, s.B, s.Nq, s.Hq, s.d, s.q_bs))) return rc;
+  if ((rc = make_map(&a.tm_k, k_blk, bf, s.B, s.Nkv, s.Hkv, s.d, s.kv_bs))) return rc;
+  if ((rc = make_map(&a.tm_v, v16, 0, s.B, s.Nkv, s.Hkv, s.d,
+                     dtype == RA_BF16 ? (long long)s.Nkv * s.Hkv * s.d : s.kv_bs)))
+    return rc;
+  a.qk_bf16 = bf;
+  a.B = s.B; a.Nq = s.Nq; a.Nkv = s.Nkv; a.Hq = s.Hq; a.Hkv = s.Hkv; a.d = s.d;
+  a.scale_log2 = scale * 1.4426950408889634f;
+  a.causal = causal != 0; a.q_off = q_off; a.kv_off = kv_off;
+  a.ring_P = 0; a.ring_S = 0; a.mode = 1;
+  a.o_acc = o_acc; a.m_acc = m_acc; a.l_acc = l_acc;
+  a.status = st;
+  a.wait_limit_ns = wait_limit_ns();
+  const int nqt = (s.Nq + 127) / 128;
+  a.num_units = s.B * s.Hq * ((nqt + 1) / 2);
+  TimedLaunch tl(RA_KERNEL_FWD_TC, cs);
+  cudaError_t e = launch_tc_fwd(a, device_sms(), cs);
+  return e == cudaSuccess ? RA_OK : cuda_fail(e, "tensor-core block forward launch");
+}
+
+size_t ra_ring_fwd_workspace_bytes(ra_dtype dtype, ra_shape shape, int P) {
+  (void)P;
+  if (dtype != RA_BF16 || shape.B < 1 || shape.N_kv < 1 || shape.Hkv < 1 || shape.d < 1) return 0;
+  return align256((size_t)shape.B * shape.N_kv * shape.Hkv * shape.d * 2);
+}
+
+static int check_ring(const Shape& s, int P, int dtype) {
+  if (s.Nq != s.Nkv) return fail(RA_ERR_INVALID_ARG, "ring attention needs N_q == N_kv (%d vs %d)", s.Nq, s.Nkv);
+  if (P < 1 || s.Nq % P) return fail(RA_ERR_INVALID_ARG, "P=%d must divide N=%d", P, s.Nq);
+  if (dtype != RA_F32 && (s.Nq / P) % 128)
+    return fail(RA_ERR_UNSUPPORTED, "tensor-core ring needs a host block N/P that is a multiple of 128 (got %d)",
+                s.Nq / P);
+  return RA_OK;
+}
+
+int ra_ring_fwd(const void* q, const void* k, const void* v, ra_dtype dtype, ra_shape shape,
+                int P, int causal, float scale, void* o, ra_dtype o_dtype, float* lse,
+                void* workspace, size_t ws_bytes, void* stream) {
+  Shape s;
+  int rc;
+  if ((rc = check_shape(shape, &s))) return rc;
+  if (!valid_dtype(dtype) || !valid_dtype(o_dtype)) return fail(RA_ERR_INVALID_ARG, "bad dtype");
+  if ((rc = check_scale(scale))) return rc;
+  if ((rc = check_ring(s, P, dtype))) return rc;
+  if ((rc = check_ptr(q, "q")) || (rc = check_ptr(k, "k")) || (rc = check_ptr(v, "v")) ||
+      (rc = check_ptr(o, "o")) || (rc = check_ptr(lse, "lse")))
+    return rc;
+  int* st;
+  if ((rc = status_ptr(&st))) return rc;
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  if (dtype == RA_F32) {
+    if (s.d != 32 && s.d != 64 && s.d != 128)
+      return fail(RA_ERR_UNSUPPORTED, "fp32 path supports d in {32, 64, 128} (got %d)", s.d);
+    SimtFwdArgs a{};
+    a.q = static_cast<const float*>(q);
+    a.k = static_cast<const float*>(k);
+    a.v = static_cast<const float*>(v);
+    a.B = s.B; a.Nq = s.Nq; a.Nkv = s.Nkv; a.Hq = s.Hq; a.Hkv = s.Hkv; a.d = s.d;
+    a.q_bs = s.q_bs; a.kv_bs = s.kv_bs;
+    a.scale = scale; a.causal = causal != 0;
+    a.P = P; a.S = s.Nq / P;
+    a.o_out = o; a.o_dtype = o_dtype; a.o_bs = s.q_bs; a.lse = lse;
+    TimedLaunch tl(RA_KERNEL_FWD_F32, cs);
+    cudaError_t e = launch_simt_fwd(a, cs);
+    return e == cudaSuccess ? RA_OK : cuda_fail(e, "fp32 ring forward launch");
+  }
+  if ((rc = check_tc(s, dtype))) return rc;
+  const void* v16 = v;
+  if (dtype == RA_BF16) {
+    const size_t need = ra_ring_fwd_workspace_bytes(dtype, shape, P);
+    if (!workspace || ws_bytes < need)
+      return fail(RA_ERR_INVALID_ARG, "workspace of %zu bytes needed (got %zu)", need, ws_bytes);
+    if ((rc = check_ptr(workspace, "workspace"))) return rc;
+    cudaError_t e = launch_to_f16(v, RA_BF16, s.kv_bs, workspace, s.B,
+                                  (long long)s.Nkv * s.Hkv * s.d, st, cs);
+    if (e != cudaSuccess) return cuda_fail(e, "v -> fp16 launch");
+    v16 = workspace;
+  }
+  TcFwdArgs a;
+  memset(&a, 0, sizeof a);
+  const int bf = dtype == RA_BF16;
+  if ((rc = make_map(&a.tm_q, q, bf, s.B, s.Nq, s.Hq, s.d, s.q_bs))) return rc;
+  if ((rc = make_map(&a.tm_k, k, bf, s.B, s.Nkv, s.Hkv, s.d, s.kv_bs))) return rc;
+  if ((rc = make_map(&a.tm_v, v16, 0, s.B, s.Nkv, s.Hkv, s.d,
+                     dtype == RA_BF16 ? (long long)s.Nkv * s.Hkv * s.d : s.kv_bs)))
+    return rc;
+  a.qk_bf16 = bf;
+  a.B = s.B; a.Nq = s.Nq; a.Nkv = s.Nkv; a.Hq = s.Hq; a.Hkv = s.Hkv; a.d = s.d;
+  a.scale_log2 = scale * 1.4426950408889634f;
+  a.causal = causal != 0;
+  a.ring_P = P; a.ring_S = s.Nq / P; a.mode = 0;
+  a.o_out = o; a.o_dtype = o_dtype; a.o_bs = s.q_bs; a.lse = lse;
+  a.status = st;
+  a.wait_limit_ns = wait_limit_ns();
+  const int T = a.ring_S / 128;
+  a.num_units = s.B * s.Hq * P * ((T + 1) / 2);
+  TimedLaunch tl(RA_KERNEL_FWD_TC, cs);
+  cudaError_t e = launch_tc_fwd(a, device_sms(), cs);
+  return e == cudaSuccess ? RA_OK : cuda_fail(e, "tensor-core ring forward launch");
+}
+
+// Backward workspace: D [B,Hq,N] fp32 | dq_acc [B,N,Hq,d] fp32 |
+// fp16 copies of q, k, v, dO (16-bit dtypes that are not already fp16).
+struct BwdWs {
+  size_t D, lse2, dq, q16, k16, v16, do16, total;
+};
+static BwdWs bwd_layout(int dtype, const ra_shape& sh) {
+  BwdWs w{};
+  const size_t qel = (size_t)sh.B * sh.N_q * sh.Hq * sh.d;
+  const size_t kvel = (size_t)sh.B * sh.N_kv * sh.Hkv * sh.d;
+  size_t off = 0;
+  w.D = off; off += align256((size_t)sh.B * sh.Hq * sh.N_q * 4);
+  if (dtype != RA_F32) {
+    w.lse2 = off; off += align256((size_t)sh.B * sh.Hq * sh.N_q * 4);
+    w.dq = off; off += align256(qel * 4);
+    if (dtype == RA_BF16) {
+      w.q16 = off; off += align256(qel * 2);
+      w.k16 = off; off += align256(kvel * 2);
+      w.v16 = off; off += align256(kvel * 2);
+      w.do16 = off; off += align256(qel * 2);
+    }
+  }
+  w.total = off;
+  return w;
+}
+
+size_t ra_ring_bwd_workspace_bytes(ra_dtype dtype, ra_dtype grad_dtype, ra_shape shape, int P) {
+  (void)grad_dtype;
+  (void)P;
+  if (shape.B < 1 || shape.N_q < 1 || shape.N_kv < 1 || shape.Hq < 1 || shape.Hkv < 1 || shape.d < 1) return 0;
+  return bwd_layout(dtype, shape).total;
+}
+
+int ra_ring_bwd(const void* q, const void* k, const void* v, const void* o, ra_dtype o_dtype,
+                const void* dO, const float* lse, ra_dtype dtype, ra_shape shape, int P,
+                int causal, float scale, void* dq, void* dk, void* dv, ra_dtype grad_dtype,
+                void* workspace, size_t ws_bytes, void* stream) {
+  Shape s;
+  int rc;
+  if ((rc = check_shape(shape, &s))) return rc;
+  if (!valid_dtype(dtype) || !valid_dtype(o_dtype) || !valid_dtype(grad_dtype))
+    return fail(RA_ERR_INVALID_ARG, "bad dtype");
+  if ((rc = check_scale(scale))) return rc;
+  if ((rc = check_ring(s, P, dtype))) return rc;
+  if ((rc = check_ptr(q, "q")) || (rc = check_ptr(k, "k")) || (rc = check_ptr(v, "v")) ||
+      (rc = check_ptr(o, "o")) || (rc = check_ptr(dO, "dO")) || (rc = check_ptr(lse, "lse")) ||
+      (rc = check_ptr(dq, "dq")) || (rc = check_ptr(dk, "dk")) || (rc = check_ptr(dv, "dv")))
+    return rc;
+  const BwdWs w = bwd_layout(dtype, shape);
+  if (!workspace || ws_bytes < w.total)
+    return fail(RA_ERR_INVALID_ARG, "workspace of %zu bytes needed (got %zu)", w.total, ws_bytes);
+  if ((rc = check_ptr(workspace, "workspace"))) return rc;
+  int* st;
+  if ((rc = status_ptr(&st))) return rc;
+  cudaStream_t cs = static_cast<cudaStream_t>(stream);
+  char* ws = static_cast<char*>(workspace);
+  float* Dv = reinterpret_cast<float*>(ws + w.D);
+  if (dtype == RA_F32) {
+    if (s.d != 32 && s.d != 64 && s.d != 128)
+      return fail(RA_ERR_UNSUPPORTED, "fp32 path supports d in {32, 64, 128} (got %d)", s.d);
+    cudaError_t e = launch_bwd_dot(dO, RA_F32, o, o_dtype, s.q_bs, Dv, nullptr, nullptr, s.B, s.Nq,
+                                   s.Hq, s.d, cs);
+    if (e != cudaSuccess) return cuda_fail(e, "bwd D launch");
+    SimtBwdArgs a{};
+    a.q = static_cast<const float*>(q);
+    a.k = static_cast<const float*>(k);
+    a.v = static_cast<const float*>(v);
+    a.dO = static_cast<const float*>(dO);
+    a.lse = lse;
+    a.Dvec = Dv;
+    a.B = s.B; a.N = s.Nq; a.Hq = s.Hq; a.Hkv = s.Hkv; a.d = s.d;
+    a.q_bs = s.q_bs; a.kv_bs = s.kv_bs;
+    a.scale = scale; a.causal = causal != 0;
+    a.P = P; a.S = s.Nq / P;
+    a.dq = dq; a.dk = dk; a.dv = dv; a.grad_dtype = grad_dtype;
+    {
+      TimedLaunch tl(RA_KERNEL_BWD_F32, cs);
+      e = launch_simt_bwd(a, cs);
+    }
+    return e == cudaSuccess ? RA_OK : cuda_fail(e, "fp32 ring backward launch");
+  }
+  if ((rc = check_tc(s, dtype))) return rc;
+  const long long qel = (long long)s.Nq * s.Hq * s.d, kvel = (long long)s.Nkv * s.Hkv * s.d;
+  float* lse2 = reinterpret_cast<float*>(ws + w.lse2);
+  cudaError_t e = launch_bwd_dot(dO, dtype, o, o_dtype, s.q_bs, Dv, lse, lse2, s.B, s.Nq, s.Hq,
+                                 s.d, cs);
+  if (e != cudaSuccess) return cuda_fail(e, "bwd D launch");
+  const void *q16 = q, *k16 = k, *v16 = v, *do16 = dO;
+  long long q16_bs = s.q_bs, kv16_bs = s.kv_bs;
+  if (dtype == RA_BF16) {
+    q16 = ws + w.q16; k16 = ws + w.k16; v16 = ws + w.v16; do16 = ws + w.do16;
+    q16_bs = qel; kv16_bs = kvel;
+    if ((e = launch_to_f16(q, RA_BF16, s.q_bs, ws + w.q16, s.B, qel, st, cs)) != cudaSuccess ||
+        (e = launch_to_f16(k, RA_BF16, s.kv_bs, ws + w.k16, s.B, kvel, st, cs)) != cudaSuccess ||
+        (e = launch_to_f16(v, RA_BF16, s.kv_bs, ws + w.v16, s.B, kvel, st, cs)) != cudaSuccess ||
+        (e = launch_to_f16(dO, RA_BF16, s.q_bs, ws + w.do16, s.B, qel, st, cs)) != cudaSuccess)
+      return cuda_fail(e, "fp16 operand copy launch");
+  }
+  float* dq_acc = reinterpret_cast<float*>(ws + w.dq);
+  e = cudaMemsetAsync(dq_acc, 0, (size_t)s.B * qel * 4, cs);
+  if (e != cudaSuccess) return cuda_fail(e, "zero dq accumulator");
+  TcBwdArgs a;
+  memset(&a, 0, sizeof a);
+  if ((rc = make_map(&a.tm_q, q16, 0, s.B, s.Nq, s.Hq, s.d, q16_bs)) ||
+      (rc = make_map(&a.tm_do, do16, 0, s.B, s.Nq, s.Hq, s.d, q16_bs)) ||
+      (rc = make_map(&a.tm_k, k16, 0, s.B, s.Nkv, s.Hkv, s.d, kv16_bs)) ||
+      (rc = make_map(&a.tm_v, v16, 0, s.B, s.Nkv, s.Hkv, s.d, kv16_bs)))
+    return rc;
+  a.B = s.B; a.N = s.Nq; a.Hq = s.Hq; a.Hkv = s.Hkv; a.d = s.d;
+  a.scale = scale;
+  a.scale_log2 = scale * 1.4426950408889634f;
+  a.causal = causal != 0;
+  a.ring_P = P; a.ring_S = s.Nq / P;
+  a.lse = lse2; a.Dvec = Dv; a.dq_acc = dq_acc;
+  a.dk = dk; a.dv = dv; a.grad_dtype = grad_dtype; a.kv_bs = s.kv_bs;
+  a.status = st;
+  a.wait_limit_ns = wait_limit_ns();
+  a.num_units = s.B * s.Hkv * (s.Nkv / 128);
+  {
+    TimedLaunch tl(RA_KERNEL_BWD_TC, cs);
+    e = launch_tc_bwd(a, device_sms(), cs);
+  }
+  if (e != cudaSuccess) return cuda_fail(e, "tensor-core ring backward launch");
+  e = launch_f32_to(dq_acc, dq, grad_dtype, s.q_bs, s.B, qel, scale, cs);
+  return e == cudaSuccess ? RA_OK : cuda_fail(e, "dq conversion launch");
+}
+
+}  // extern "C"

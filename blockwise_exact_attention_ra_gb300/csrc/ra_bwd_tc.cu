@@ -1,0 +1,486 @@
+// Backward blockwise attention on the sm_103a tensor cores (tcgen05 + TMEM +
+// TMA).
+//
+// What it computes: the gradients of L = sum(O * dO) for exact attention,
+// with the probabilities recomputed from the saved LSE rather than stored
+// (activation recomputation; "Ring Attention: Train 1M Tokens on 8GB GPUs in
+// 2026", "Building Ring Attention in PyTorch: The 200-Line Version").  Each
+// key/value tile keeps its dK, dV accumulators in TMEM while it travels the
+// ring: block j visits hosts (j + s) mod P, s = 0, 1, ... (its gradients
+// "flow backwards through the ring", section "Gotchas and Failure Modes"),
+// skipping hosts wholly before it under a causal mask.  Per visited query
+// tile i:
+//   S^T  = K Q_i^T                    (recompute)
+//   P^T  = exp(scale S^T - LSE_i)     (masked on the diagonal tile)
+//   dP^T = V dO_i^T
+//   dS^T = P^T * (dP^T - D_i),        D_i = rowsum(dO_i * O_i)
+//   dV  += P^T dO_i ;  dK += dS^T Q_i ;  dQ_i += dS K   (dQ reduce-added)
+// dK is scaled by `scale` at the end, dQ when it is converted.
+//
+// CTA organisation (one persistent CTA per SM, 14 warps):
+//   warp 0       TMA producer: K, V of the unit; Q_i, dO_i (+ LSE, D slices)
+//                through two shared-memory stages
+//   warp 1       TMEM allocation; one lane issues every tcgen05.mma
+//   warps 2-9    compute: thread = key row; warps 2-5 take query columns
+//                0-63, warps 6-9 columns 64-127
+//   warps 10-13  dQ: read dQ_i from TMEM (thread = query row) and reduce-add
+//                it into the fp32 accumulator; at the end of a unit write
+//                dK, dV
+// TMEM (512 columns): S^T [0,128) (P^T as fp16 written back into columns
+// [0,32) and [64,96)), dP^T [128,256) (dQ_i reuses [128,128+D)),
+// dK [256,256+D), dV [256+D,256+2D).
+// MMA order per iteration: dV(i) S(i+1) dK(i) dQ(i) dP(i+1); the compute
+// warps start on S(i+1) while dK(i) and dQ(i) run.
+#include <math.h>
+
+#include "ra_device.cuh"
+
+namespace ra {
+namespace {
+
+constexpr int kThreads = 448;
+
+template <int D>
+struct BwdSmem {
+  static constexpr int kTile = 128 * D * 2;
+  static constexpr int kK = 0;
+  static constexpr int kV = kTile;
+  static constexpr int kQ0 = 2 * kTile;      // Q stage s at kQ0 + s * kTile
+  static constexpr int kDO0 = 4 * kTile;     // dO stage s
+  static constexpr int kDS = 6 * kTile;      // dS^T, 128 key rows x 128 query columns fp16
+  static constexpr int kDSBytes = 128 * 128 * 2;
+  static constexpr int kVec0 = kDS + kDSBytes;  // per stage: LSE*log2e [128], D [128]
+  static constexpr int kBars = kVec0 + 2 * 1024;
+  // kv_full, kv_empty, qd_full[2], qd_empty[2], s_full, dp_full, ds_full,
+  // ds_free, dq_full, dq_free, dkv_full, dkv_free, drain
+  static constexpr int kNumBars = 15;
+  static constexpr int kMisc = kBars + kNumBars * 8;
+  static constexpr int kUsed = kMisc + 16;
+  // at least 120 KB so that one CTA (holding all 512 TMEM columns) occupies an SM
+  static constexpr int kBytes = kUsed > 122880 ? kUsed : 122880;
+};
+
+struct BwdUnit {
+  int b, g, jt;
+  int count;  // query tiles per head
+  int n_iter; // count * group
+};
+
+__device__ __forceinline__ BwdUnit bwd_unit(const TcBwdArgs& a, int u) {
+  BwdUnit r;
+  const int BG = a.B * a.Hkv;
+  const int bg = u % BG;
+  r.jt = u / BG;  // ascending: under a causal mask the earliest keys have the most work
+  r.b = bg / a.Hkv;
+  r.g = bg % a.Hkv;
+  const int nT = a.N / 128;
+  r.count = a.causal ? nT - r.jt : nT;
+  r.n_iter = r.count * (a.Hq / a.Hkv);
+  return r;
+}
+
+// Query head and query tile of iteration it, in ring order.
+__device__ __forceinline__ void bwd_iter(const TcBwdArgs& a, const BwdUnit& u, int it, int* h,
+                                         int* qt) {
+  const int group = a.Hq / a.Hkv;
+  const int hh = it / u.count, k = it % u.count;
+  *h = u.g * group + hh;
+  if (a.causal) {
+    *qt = u.jt + k;
+  } else {
+    const int nT = a.N / 128;
+    const int T = a.ring_S / 128;
+    const int hj = u.jt / T;
+    *qt = (hj * T + k) % nT;
+  }
+}
+
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes,
+                                          uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          dst),
+      "l"(src), "r"(bytes), "r"(bar)
+      : "memory");
+}
+
+__device__ __forceinline__ void red_add_v4(float* p, float a, float b, float c, float d) {
+  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(a), "f"(b), "f"(c),
+               "f"(d)
+               : "memory");
+}
+
+__device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t n) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_constant__ TcBwdArgs a) {
+  using L = BwdSmem<D>;
+  extern __shared__ __align__(1024) uint8_t smem[];
+  const uint32_t sbase = smem_u32(smem);
+  if (sbase & 1023u) {  // the swizzled tiles need 1024-byte alignment
+    if (threadIdx.x == 0) report(a.status, RA_ERR_UNSUPPORTED);
+    return;
+  }
+  const uint32_t bar0 = sbase + L::kBars;
+  const uint32_t BAR_KV_FULL = bar0, BAR_KV_EMPTY = bar0 + 8;
+  auto bar_qd_full = [&](int s) { return bar0 + 16 + 8 * s; };
+  auto bar_qd_empty = [&](int s) { return bar0 + 32 + 8 * s; };
+  const uint32_t BAR_S_FULL = bar0 + 48, BAR_DP_FULL = bar0 + 56, BAR_DS_FULL = bar0 + 64,
+                 BAR_DS_FREE = bar0 + 72, BAR_DQ_FULL = bar0 + 80, BAR_DQ_FREE = bar0 + 88,
+                 BAR_DKV_FULL = bar0 + 96, BAR_DKV_FREE = bar0 + 104, BAR_DRAIN = bar0 + 112;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kMisc);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kMisc + 4);
+  const uint32_t warp = warp_id();
+  const uint32_t lane = lane_id();
+  const int group = a.Hq / a.Hkv;
+
+  if (threadIdx.x == 0) {
+    mbar_init(BAR_KV_FULL, 1);
+    mbar_init(BAR_KV_EMPTY, 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(bar_qd_full(s), 1);
+      mbar_init(bar_qd_empty(s), 1);
+    }
+    mbar_init(BAR_S_FULL, 1);
+    mbar_init(BAR_DP_FULL, 1);
+    mbar_init(BAR_DS_FULL, 256);
+    mbar_init(BAR_DS_FREE, 1);
+    mbar_init(BAR_DQ_FULL, 1);
+    mbar_init(BAR_DQ_FREE, 128);
+    mbar_init(BAR_DKV_FULL, 1);
+    mbar_init(BAR_DKV_FREE, 128);
+    mbar_init(BAR_DRAIN, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), 512);
+    tmem_relinquish();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&a.tm_q);
+    tma_prefetch_desc(&a.tm_k);
+    tma_prefetch_desc(&a.tm_v);
+    tma_prefetch_desc(&a.tm_do);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const uint64_t lim = a.wait_limit_ns;
+  const uint32_t T_S = tmem, T_DP = tmem + 128, T_DK = tmem + 256, T_DV = tmem + 256 + D;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      const uint64_t pol_kv = policy_evict_first();
+      const uint64_t pol_q = policy_evict_last();
+      uint32_t qd_cnt = 0;
+      int k = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; u < a.num_units && ok; u += gridDim.x, ++k) {
+        const BwdUnit bu = bwd_unit(a, u);
+        if (!mbar_wait(BAR_KV_EMPTY, (k & 1) ^ 1, abort_flag, a.status, lim)) { ok = false; break; }
+        mbar_arrive_expect_tx(BAR_KV_FULL, 2 * L::kTile);
+#pragma unroll
+        for (int c = 0; c < D / 64; ++c) {
+          tma_load_4d(sbase + L::kK + c * 16384, &a.tm_k, BAR_KV_FULL, c * 64, bu.g, bu.jt * 128, bu.b, pol_kv);
+          tma_load_4d(sbase + L::kV + c * 16384, &a.tm_v, BAR_KV_FULL, c * 64, bu.g, bu.jt * 128, bu.b, pol_kv);
+        }
+        for (int it = 0; it < bu.n_iter; ++it) {
+          int h, qt;
+          bwd_iter(a, bu, it, &h, &qt);
+          const int s = qd_cnt & 1;
+          if (!mbar_wait(bar_qd_empty(s), ((qd_cnt >> 1) & 1) ^ 1, abort_flag, a.status, lim)) { ok = false; break; }
+          mbar_arrive_expect_tx(bar_qd_full(s), 2 * L::kTile + 1024);
+#pragma unroll
+          for (int c = 0; c < D / 64; ++c) {
+            tma_load_4d(sbase + L::kQ0 + s * L::kTile + c * 16384, &a.tm_q, bar_qd_full(s), c * 64, h, qt * 128, bu.b, pol_q);
+            tma_load_4d(sbase + L::kDO0 + s * L::kTile + c * 16384, &a.tm_do, bar_qd_full(s), c * 64, h, qt * 128, bu.b, pol_q);
+          }
+          const long long vrow = ((long long)bu.b * a.Hq + h) * a.N + (long long)qt * 128;
+          bulk_load(sbase + L::kVec0 + s * 1024, a.lse + vrow, 512, bar_qd_full(s));
+          bulk_load(sbase + L::kVec0 + s * 1024 + 512, a.Dvec + vrow, 512, bar_qd_full(s));
+          ++qd_cnt;
+        }
+      }
+      if (*abort_flag) {
+        const uint64_t drain = 100000000ull;
+        (void)mbar_wait(BAR_KV_FULL, (k - 1) & 1, abort_flag, nullptr, drain);
+        for (int s = 0; s < 2; ++s)
+          if (qd_cnt > (uint32_t)s) {
+            const uint32_t last = ((qd_cnt - 1 - s) & ~1u) + s;  // last load issued on stage s
+            (void)mbar_wait(bar_qd_full(s), (last >> 1) & 1, abort_flag, nullptr, drain);
+          }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      // S^T = K Q^T, dP^T = V dO^T: A, B K-major (M = keys, N = queries)
+      const uint32_t id_kq = idesc_f16(0, 0, 0, 128, 128);
+      // dV += P^T dO (A from TMEM), dK += dS^T Q: B MN-major (N = head dim)
+      const uint32_t id_acc = idesc_f16(0, 0, 1, 128, D);
+      // dQ = dS K: A = dS^T viewed MN-major (M = queries), B = K MN-major
+      const uint32_t id_dq = idesc_f16(0, 1, 1, 128, D);
+      const uint32_t sK = sbase + L::kK, sV = sbase + L::kV, sDS = sbase + L::kDS;
+      uint32_t qd_cnt = 0, ds_cnt = 0, dq_cnt = 0;
+      int k = 0;
+      bool ok = true;
+      auto mma_nt = [&](uint32_t dt, uint32_t sa, uint32_t sb) {  // K-major A and B, K = D
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+          mma_ss(dt, smem_desc_sw128(sa + off, 16, 1024), smem_desc_sw128(sb + off, 16, 1024), id_kq, kk > 0);
+        }
+      };
+      auto wait = [&](uint32_t bar, uint32_t par) {
+        if (!mbar_wait(bar, par, abort_flag, a.status, lim)) ok = false;
+        tc_fence_after();
+        return ok;
+      };
+      for (int u = blockIdx.x; u < a.num_units && ok; u += gridDim.x, ++k) {
+        const BwdUnit bu = bwd_unit(a, u);
+        if (!wait(BAR_KV_FULL, k & 1)) break;
+        // prologue: S(0), dP(0)
+        uint32_t s = qd_cnt & 1;
+        if (!wait(bar_qd_full(s), (qd_cnt >> 1) & 1)) break;
+        mma_nt(T_S, sK, sbase + L::kQ0 + s * L::kTile);
+        mma_commit(BAR_S_FULL);
+        if (dq_cnt > 0 && !wait(BAR_DQ_FREE, (dq_cnt - 1) & 1)) break;
+        mma_nt(T_DP, sV, sbase + L::kDO0 + s * L::kTile);
+        mma_commit(BAR_DP_FULL);
+        for (int it = 0; it < bu.n_iter; ++it) {
+          const uint32_t sQ = sbase + L::kQ0 + s * L::kTile, sDO = sbase + L::kDO0 + s * L::kTile;
+          if (!wait(BAR_DS_FULL, ds_cnt & 1)) break;
+          ++ds_cnt;
+          if (it == 0 && k > 0 && !wait(BAR_DKV_FREE, (k - 1) & 1)) break;
+          // dV += P^T dO_i   (P^T in TMEM: queries 0-63 at columns 0-31, 64-127 at 64-95)
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk) {
+            const uint32_t pa = T_S + (kk < 4 ? kk * 8 : 64 + (kk - 4) * 8);
+            mma_ts(T_DV, pa, smem_desc_sw128(sDO + kk * 2048, 16384, 1024), id_acc, (it > 0 || kk > 0) ? 1u : 0u);
+          }
+          const bool has_next = it + 1 < bu.n_iter;
+          const uint32_t s2 = (qd_cnt + 1) & 1;
+          if (has_next) {
+            if (!wait(bar_qd_full(s2), ((qd_cnt + 1) >> 1) & 1)) break;
+            mma_nt(T_S, sK, sbase + L::kQ0 + s2 * L::kTile);
+            mma_commit(BAR_S_FULL);
+          }
+          // dK += dS^T Q_i   (dS^T K-major: key rows of 64-query swizzled halves)
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk) {
+            const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+            mma_ss(T_DK, smem_desc_sw128(sDS + off, 16, 1024), smem_desc_sw128(sQ + kk * 2048, 16384, 1024), id_acc,
+                   (it > 0 || kk > 0) ? 1u : 0u);
+          }
+          // dQ_i = dS K   (the same dS^T tile read MN-major: M = queries)
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk) {
+            mma_ss(T_DP, smem_desc_sw128(sDS + kk * 2048, 16384, 1024), smem_desc_sw128(sK + kk * 2048, 16384, 1024),
+                   id_dq, kk > 0 ? 1u : 0u);
+          }
+          mma_commit(BAR_DQ_FULL);
+          ++dq_cnt;
+          mma_commit(BAR_DS_FREE);
+          mma_commit(bar_qd_empty(s));
+          ++qd_cnt;
+          if (has_next) {
+            if (!wait(BAR_DQ_FREE, (dq_cnt - 1) & 1)) break;
+            mma_nt(T_DP, sV, sbase + L::kDO0 + s2 * L::kTile);
+            mma_commit(BAR_DP_FULL);
+            s = s2;
+          } else {
+            mma_commit(BAR_DKV_FULL);
+            mma_commit(BAR_KV_EMPTY);
+          }
+        }
+      }
+      mma_commit(BAR_DRAIN);
+      (void)mbar_wait(BAR_DRAIN, 0, abort_flag, nullptr, 100000000ull);
+    }
+  } else if (warp < 10) {
+    // ------------------------------------------------------------ compute
+    const int half = (warp - 2) / 4;           // query columns [64*half, 64*half + 64)
+    const uint32_t quarter = warp & 3;
+    const int r = quarter * 32 + lane;         // key row in the tile
+    const uint32_t lane_off = (quarter * 32) << 16;
+    const uint32_t tS = T_S + lane_off + half * 64;
+    const uint32_t tDP = T_DP + lane_off + half * 64;
+    const float sl2 = a.scale_log2;
+    uint8_t* ds_row = smem + L::kDS + half * 16384 + r * 128;
+    uint32_t gi = 0;  // iterations done by this CTA (all units)
+    bool ok = true;
+    for (int u = blockIdx.x; u < a.num_units && ok; u += gridDim.x) {
+      const BwdUnit bu = bwd_unit(a, u);
+      for (int it = 0; it < bu.n_iter; ++it, ++gi) {
+        int h, qt;
+        bwd_iter(a, bu, it, &h, &qt);
+        const int s = gi & 1;
+        const float* lse2 = reinterpret_cast<const float*>(smem + L::kVec0 + s * 1024) + half * 64;
+        const float* dvec = lse2 + 128;
+        if (!mbar_wait(BAR_S_FULL, gi & 1, abort_flag, a.status, lim)) { ok = false; break; }
+        // the LSE / D slices of this stage arrived with the Q tile
+        if (!mbar_wait(bar_qd_full(s), (gi >> 1) & 1, abort_flag, a.status, lim)) { ok = false; break; }
+        tc_fence_after();
+        uint32_t pr[64];
+        RA_TMEM_LD32(tS, pr);
+        RA_TMEM_LD32(tS + 32, (pr + 32));
+        tmem_ld_wait();
+        const bool diag = a.causal && qt == bu.jt;
+        // P^T = exp2(S^T * scale*log2e - LSE*log2e); query column c visible iff c >= key row
+#pragma unroll
+        for (int c = 0; c < 64; ++c) {
+          float p = ex2_approx(fmaf(__uint_as_float(pr[c]), sl2, -lse2[c]));
+          if (diag && half * 64 + c < r) p = 0.f;
+          pr[c] = __float_as_uint(p);
+        }
+        // P^T (fp16) back into TMEM for the dV MMA
+#pragma unroll
+        for (int c = 0; c < 64; c += 32) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int j = 0; j < 32; j += 2) pk[j / 2] = pack_half2(__uint_as_float(pr[c + j]), __uint_as_float(pr[c + j + 1]));
+          RA_TMEM_ST16(tS + c / 2, pk);
+        }
+        if (!mbar_wait(BAR_DP_FULL, gi & 1, abort_flag, a.status, lim)) { ok = false; break; }
+        tc_fence_after();
+        // dS^T of the previous iteration must have been consumed by its MMAs
+        if (gi > 0 && !mbar_wait(BAR_DS_FREE, (gi - 1) & 1, abort_flag, a.status, lim)) { ok = false; break; }
+#pragma unroll
+        for (int c = 0; c < 64; c += 32) {
+          uint32_t dp[32];
+          RA_TMEM_LD32(tDP + c, dp);
+          tmem_ld_wait();
+          uint32_t pk[16];
+#pragma unroll
+          for (int j = 0; j < 32; j += 2) {
+            const float d0 = __uint_as_float(pr[c + j]) * (__uint_as_float(dp[j]) - dvec[c + j]);
+            const float d1 = __uint_as_float(pr[c + j + 1]) * (__uint_as_float(dp[j + 1]) - dvec[c + j + 1]);
+            pk[j / 2] = pack_half2(d0, d1);
+          }
+          // 16-byte chunks (c/8 .. c/8+3) of this row, 128-byte swizzle
+#pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4) {
+            const int chunk = (c >> 3) + q4;
+            *reinterpret_cast<uint4*>(ds_row + ((chunk ^ (r & 7)) << 4)) =
+                make_uint4(pk[4 * q4], pk[4 * q4 + 1], pk[4 * q4 + 2], pk[4 * q4 + 3]);
+          }
+        }
+        fence_proxy_async_smem();
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(BAR_DS_FULL);
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ dQ / epilogue
+    const uint32_t quarter = warp & 3;
+    const int r = quarter * 32 + lane;
+    const uint32_t lane_off = (quarter * 32) << 16;
+    uint32_t dq_cnt = 0;
+    int k = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; u < a.num_units && ok; u += gridDim.x, ++k) {
+      const BwdUnit bu = bwd_unit(a, u);
+      for (int it = 0; it < bu.n_iter; ++it) {
+        int h, qt;
+        bwd_iter(a, bu, it, &h, &qt);
+        if (!mbar_wait(BAR_DQ_FULL, dq_cnt & 1, abort_flag, a.status, lim)) { ok = false; break; }
+        ++dq_cnt;
+        tc_fence_after();
+        float* dst = a.dq_acc + (((long long)bu.b * a.N + (long long)qt * 128 + r) * a.Hq + h) * D;
+#pragma unroll
+        for (int c = 0; c < D; c += 64) {
+          uint32_t v[64];
+          RA_TMEM_LD32(T_DP + lane_off + c, v);
+          RA_TMEM_LD32(T_DP + lane_off + c + 32, (v + 32));
+          tmem_ld_wait();
+          if (c + 64 >= D) {
+            tc_fence_before();
+            mbar_arrive(BAR_DQ_FREE);
+          }
+#pragma unroll
+          for (int j = 0; j < 64; j += 4)
+            red_add_v4(dst + c + j, __uint_as_float(v[j]), __uint_as_float(v[j + 1]), __uint_as_float(v[j + 2]),
+                       __uint_as_float(v[j + 3]));
+        }
+      }
+      if (!ok) break;
+      if (!mbar_wait(BAR_DKV_FULL, k & 1, abort_flag, a.status, lim)) { ok = false; break; }
+      tc_fence_after();
+      const long long row = (long long)bu.jt * 128 + r;
+      const long long base = bu.b * a.kv_bs + (row * a.Hkv + bu.g) * D;
+#pragma unroll
+      for (int which = 0; which < 2; ++which) {
+        const uint32_t src = (which == 0 ? T_DK : T_DV) + lane_off;
+        const float mul = which == 0 ? a.scale : 1.f;
+        void* outp = which == 0 ? a.dk : a.dv;
+#pragma unroll
+        for (int c = 0; c < D; c += 32) {
+          uint32_t v[32];
+          RA_TMEM_LD32(src + c, v);
+          tmem_ld_wait();
+          if (a.grad_dtype == RA_F32) {
+            float* op = static_cast<float*>(outp) + base + c;
+#pragma unroll
+            for (int j = 0; j < 32; j += 4)
+              *reinterpret_cast<float4*>(op + j) =
+                  make_float4(__uint_as_float(v[j]) * mul, __uint_as_float(v[j + 1]) * mul,
+                              __uint_as_float(v[j + 2]) * mul, __uint_as_float(v[j + 3]) * mul);
+          } else {
+            uint32_t pk[16];
+#pragma unroll
+            for (int j = 0; j < 32; j += 2) {
+              const float f0 = __uint_as_float(v[j]) * mul, f1 = __uint_as_float(v[j + 1]) * mul;
+              if (a.grad_dtype == RA_BF16) {
+                __nv_bfloat162 t = __floats2bfloat162_rn(f0, f1);
+                pk[j / 2] = *reinterpret_cast<uint32_t*>(&t);
+              } else {
+                pk[j / 2] = pack_half2(f0, f1);
+              }
+            }
+            uint4* op = reinterpret_cast<uint4*>(static_cast<uint16_t*>(outp) + base + c);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) op[j] = make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+          }
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(BAR_DKV_FREE);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem, 512);
+}
+
+}  // namespace
+
+cudaError_t launch_tc_bwd(TcBwdArgs& a, int num_sms, cudaStream_t st) {
+  if (a.num_units <= 0) return cudaSuccess;
+  const int grid = a.num_units < num_sms ? a.num_units : num_sms;
+  cudaError_t e;
+  if (a.d == 128) {
+    e = cudaFuncSetAttribute(tc_bwd_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             BwdSmem<128>::kBytes);
+    if (e != cudaSuccess) return e;
+    tc_bwd_kernel<128><<<grid, kThreads, BwdSmem<128>::kBytes, st>>>(a);
+  } else if (a.d == 64) {
+    e = cudaFuncSetAttribute(tc_bwd_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             BwdSmem<64>::kBytes);
+    if (e != cudaSuccess) return e;
+    tc_bwd_kernel<64><<<grid, kThreads, BwdSmem<64>::kBytes, st>>>(a);
+  } else {
+    return cudaErrorInvalidValue;
+  }
+  count_launch();
+  return cudaGetLastError();
+}
+
+}  // namespace ra

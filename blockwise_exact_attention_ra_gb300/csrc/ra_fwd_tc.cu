@@ -1,0 +1,537 @@
+// Forward blockwise attention on the sm_103a tensor cores (tcgen05 + TMEM +
+// TMA), for the ring of virtual hosts and for a single (Q block, KV block)
+// step.
+//
+// What it computes: for every query row, the online-softmax state over the
+// key/value tiles it sees, visited in ring order -- host i takes key/value
+// blocks (i - s) mod P, s = 0, 1, ... ("Ring Attention: Train 1M Tokens on
+// 8GB GPUs in 2026", section "Ring Attention: Partition Sequence Length, Not
+// Batch"), each block's tiles from the last to the first -- merged with the
+// rescaled (max, exp_sum, weighted_output) rule of its "Gotchas and Failure
+// Modes" section, then normalised (O = o / l, LSE = m + ln l).  Blocks wholly
+// in a query tile's causal future are skipped; only tiles that straddle the
+// diagonal (or the ragged end of a block) are masked element by element.
+//
+// CTA organisation (one persistent CTA per SM, 10 warps):
+//   warp 0      TMA producer: Q tiles of the unit, then K(0), V(0), K(1), ...
+//               through a ring of shared-memory stages
+//   warp 1      allocates TMEM; one lane issues every tcgen05.mma
+//   warps 2-5   softmax warpgroup for query tile A (thread = row)
+//   warps 6-9   softmax warpgroup for query tile B (the next 128 rows)
+// A unit is a pair of 128-row query tiles of one (batch, head) in one host,
+// so every K/V tile brought into shared memory feeds two tiles of MMAs.
+//
+// TMEM (512 columns x 128 lanes, fp32): S_A [0,128) S_B [128,256)
+// O_A [256, 256+D) O_B [256+D, 256+2D).  The softmax warps overwrite the
+// first 64 columns of S_X with P_X as packed fp16 pairs, which the PV MMA
+// reads directly from TMEM (A operand), so P never touches shared memory.
+// The MMA order per iteration is  PV_A(it) S_A(it+1) PV_B(it) S_B(it+1):
+// while one warpgroup computes its softmax the tensor core works on the
+// other tile.
+//
+// Numerics: S = Q K^T accumulates in fp32 from bf16/fp16 operands; scores
+// are scaled in the exponent (exp2 with log2(e) folded into the scale);
+// P is rounded to fp16 and V is fp16, O accumulates in fp32.  The running
+// maximum is updated lazily: O and l are rescaled only when the maximum
+// grows by more than 8 (log2 units), so P <= 2^8, well inside fp16.
+#include <math.h>
+
+#include "ra_device.cuh"
+
+namespace ra {
+namespace {
+
+constexpr int kThreads = 320;
+constexpr int kStages = 4;
+constexpr float kRescaleThreshold = 8.0f;
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kLog2e = 1.4426950408889634f;
+
+template <int D>
+struct FwdSmem {
+  static constexpr int kTileBytes = 128 * D * 2;  // one 128-row tile, fp16/bf16
+  static constexpr int kQA = 0;
+  static constexpr int kQB = kTileBytes;
+  static constexpr int kStage0 = 2 * kTileBytes;
+  static constexpr int kBars = kStage0 + kStages * kTileBytes;
+  // barriers: q_full, q_empty, kv_full[S], kv_empty[S], s_full[2], p_full[2],
+  // o_full[2], drain
+  static constexpr int kNumBars = 2 + 2 * kStages + 6 + 1;
+  static constexpr int kMisc = kBars + kNumBars * 8;  // tmem slot, abort flag
+  static constexpr int kBytes = kMisc + 16;
+  // slack for 1024-byte alignment; at least 120 KB so that one CTA (holding
+  // all 512 TMEM columns) occupies an SM
+  static constexpr int kAlloc = (kBytes + 1024) > 122880 ? (kBytes + 1024) : 122880;
+};
+
+struct UnitInfo {
+  int b, h, g;
+  int qa_row0;    // tensor row of tile A (tile B = qa_row0 + 128)
+  int has_b;
+  int n_iter;     // key/value tiles visited
+  int start[2];   // first iteration at which tile A / B is active
+  long long qpos0[2];  // global position of row 0 of tile A / B
+  // key/value tile at iteration it:
+  //   kt = ring_noncausal ? (kt0 - it) mod nkt : kt0 - it
+  int kt0;
+  int nkt;
+  int wrap;
+};
+
+__device__ __forceinline__ int kt_at(const UnitInfo& u, int it) {
+  int kt = u.kt0 - it;
+  if (u.wrap && kt < 0) kt += u.nkt;
+  return kt;
+}
+
+// Last key/value tile with at least one key visible to some row of a query
+// tile whose first row is at position qpos0 and last valid row at qpos_last.
+__device__ __forceinline__ int last_visible_tile(const TcFwdArgs& a, long long qpos_last,
+                                                 int nkt) {
+  if (!a.causal) return nkt - 1;
+  const long long lim = qpos_last - a.kv_off;  // keys at row index <= lim are visible
+  if (lim < 0) return -1;
+  const long long t = lim / 128;
+  return (int)(t < nkt - 1 ? t : nkt - 1);
+}
+
+__device__ __forceinline__ UnitInfo unit_info(const TcFwdArgs& a, int u) {
+  UnitInfo r;
+  const int BH = a.B * a.Hq;
+  const int bh = u % BH;
+  const int pidx_desc = u / BH;
+  r.b = bh / a.Hq;
+  r.h = bh % a.Hq;
+  r.g = r.h / (a.Hq / a.Hkv);
+  const int nkt = (a.Nkv + 127) / 128;
+  r.nkt = nkt;
+  if (a.ring_P > 0) {
+    const int T = a.ring_S / 128;
+    const int pph = (T + 1) / 2;
+    const int total = a.ring_P * pph;
+    const int pg = total - 1 - pidx_desc;  // heaviest (latest) pairs first
+    const int host = pg / pph, lp = pg % pph;
+    r.qa_row0 = host * a.ring_S + lp * 256;
+    r.has_b = (2 * lp + 1) < T;
+    const int ta = r.qa_row0 / 128;
+    const int lead = r.has_b ? ta + 1 : ta;
+    r.qpos0[0] = r.qa_row0;
+    r.qpos0[1] = r.qa_row0 + 128;
+    if (a.causal) {
+      r.kt0 = lead;
+      r.n_iter = lead + 1;
+      r.wrap = 0;
+      r.start[0] = lead - ta;
+      r.start[1] = 0;
+    } else {
+      r.kt0 = (host + 1) * T - 1;
+      r.n_iter = nkt;
+      r.wrap = 1;
+      r.start[0] = 0;
+      r.start[1] = 0;
+    }
+  } else {
+    const int nqt = (a.Nq + 127) / 128;
+    const int total = (nqt + 1) / 2;
+    const int lp = total - 1 - pidx_desc;
+    r.qa_row0 = lp * 256;
+    r.has_b = (r.qa_row0 + 128) < a.Nq;
+    r.qpos0[0] = a.q_off + r.qa_row0;
+    r.qpos0[1] = a.q_off + r.qa_row0 + 128;
+    const long long lastA = a.q_off + min(r.qa_row0 + 127, a.Nq - 1);
+    const int ktA = last_visible_tile(a, lastA, nkt);
+    int ktB = -1;
+    if (r.has_b) ktB = last_visible_tile(a, a.q_off + min(r.qa_row0 + 255, a.Nq - 1), nkt);
+    const int lead = r.has_b ? max(ktA, ktB) : ktA;
+    r.kt0 = lead;
+    r.n_iter = lead + 1;
+    r.wrap = 0;
+    r.start[0] = ktA >= 0 ? lead - ktA : r.n_iter;      // never active if no key visible
+    r.start[1] = r.has_b ? (ktB >= 0 ? lead - ktB : r.n_iter) : r.n_iter;
+  }
+  if (!r.has_b) r.start[1] = r.n_iter;
+  return r;
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_constant__ TcFwdArgs a) {
+  using L = FwdSmem<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  const uint32_t sbase = smem_u32(smem);
+  const uint32_t bar0 = sbase + L::kBars;
+  const uint32_t BAR_Q_FULL = bar0, BAR_Q_EMPTY = bar0 + 8;
+  auto bar_kv_full = [&](int s) { return bar0 + 16 + 8 * s; };
+  auto bar_kv_empty = [&](int s) { return bar0 + 16 + 8 * kStages + 8 * s; };
+  const uint32_t bar_x = bar0 + 16 + 16 * kStages;
+  auto bar_s_full = [&](int x) { return bar_x + 8 * x; };
+  auto bar_p_full = [&](int x) { return bar_x + 16 + 8 * x; };
+  auto bar_o_full = [&](int x) { return bar_x + 32 + 8 * x; };
+  const uint32_t BAR_DRAIN = bar_x + 48;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kMisc);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kMisc + 4);
+
+  const uint32_t warp = warp_id();
+  const uint32_t lane = lane_id();
+
+  if (threadIdx.x == 0) {
+    mbar_init(BAR_Q_FULL, 1);
+    mbar_init(BAR_Q_EMPTY, 1);
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(bar_kv_full(s), 1);
+      mbar_init(bar_kv_empty(s), 1);
+    }
+    for (int x = 0; x < 2; ++x) {
+      mbar_init(bar_s_full(x), 1);
+      mbar_init(bar_p_full(x), 128);
+      mbar_init(bar_o_full(x), 1);
+    }
+    mbar_init(BAR_DRAIN, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), 512);
+    tmem_relinquish();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&a.tm_q);
+    tma_prefetch_desc(&a.tm_k);
+    tma_prefetch_desc(&a.tm_v);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const uint64_t lim = a.wait_limit_ns;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      const uint64_t pol_kv = policy_evict_last();
+      const uint64_t pol_q = policy_evict_first();
+      uint32_t L_cnt = 0;  // K/V loads issued
+      int k = 0;
+      bool ok = true;
+      uint32_t last_phase[kStages];
+      int issued[kStages];
+      for (int s = 0; s < kStages; ++s) issued[s] = 0, last_phase[s] = 0;
+      int q_issued = 0;
+      for (int u = blockIdx.x; u < a.num_units && ok; u += gridDim.x) {
+        const UnitInfo ui = unit_info(a, u);
+        if (ui.n_iter == 0) continue;  // no key of this block is visible to the unit
+        if (!mbar_wait(BAR_Q_EMPTY, (k & 1) ^ 1, abort_flag, a.status, lim)) { ok = false; break; }
+        ++k;
+        const uint32_t qbytes = (ui.has_b ? 2 : 1) * L::kTileBytes;
+        mbar_arrive_expect_tx(BAR_Q_FULL, qbytes);
+        q_issued = 1;
+#pragma unroll
+        for (int c = 0; c < D / 64; ++c) {
+          tma_load_4d(sbase + L::kQA + c * 16384, &a.tm_q, BAR_Q_FULL, c * 64, ui.h,
+                      ui.qa_row0, ui.b, pol_q);
+          if (ui.has_b)
+            tma_load_4d(sbase + L::kQB + c * 16384, &a.tm_q, BAR_Q_FULL, c * 64, ui.h,
+                        ui.qa_row0 + 128, ui.b, pol_q);
+        }
+        for (int it = 0; it < ui.n_iter && ok; ++it) {
+          const int kt = kt_at(ui, it);
+#pragma unroll
+          for (int kv = 0; kv < 2; ++kv) {  // K then V
+            const int s = L_cnt % kStages;
+            const uint32_t ph = (L_cnt / kStages) & 1;
+            if (!mbar_wait(bar_kv_empty(s), ph ^ 1, abort_flag, a.status, lim)) { ok = false; break; }
+            mbar_arrive_expect_tx(bar_kv_full(s), L::kTileBytes);
+            const CUtensorMap* tm = kv == 0 ? &a.tm_k : &a.tm_v;
+#pragma unroll
+            for (int c = 0; c < D / 64; ++c)
+              tma_load_4d(sbase + L::kStage0 + s * L::kTileBytes + c * 16384, tm,
+                          bar_kv_full(s), c * 64, ui.g, kt * 128, ui.b, pol_kv);
+            issued[s] = 1;
+            last_phase[s] = ph;
+            ++L_cnt;
+          }
+        }
+      }
+      if (*abort_flag) {
+        // let copies already in flight land before the CTA exits
+        const uint64_t drain = 100000000ull;
+        for (int s = 0; s < kStages; ++s)
+          if (issued[s]) (void)mbar_wait(bar_kv_full(s), last_phase[s], abort_flag, nullptr, drain);
+        if (q_issued) (void)mbar_wait(BAR_Q_FULL, (k - 1) & 1, abort_flag, nullptr, drain);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      const uint32_t idesc_qk = idesc_f16(a.qk_bf16 ? 1u : 0u, 0, 0, 128, 128);
+      const uint32_t idesc_pv = idesc_f16(0, 0, 1, 128, D);
+      const uint32_t tS[2] = {tmem + 0u, tmem + 128u};
+      const uint32_t tO[2] = {tmem + 256u, tmem + 256u + (uint32_t)D};
+      uint32_t L_cnt = 0;
+      uint32_t p_cnt[2] = {0, 0};
+      int k = 0;
+      bool ok = true;
+      auto issue_s = [&](int x, uint32_t kstage) {
+        const uint32_t qa = sbase + (x == 0 ? L::kQA : L::kQB);
+        const uint32_t kb = sbase + L::kStage0 + kstage * L::kTileBytes;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+          mma_ss(tS[x], smem_desc_sw128(qa + off, 16, 1024), smem_desc_sw128(kb + off, 16, 1024),
+                 idesc_qk, kk > 0);
+        }
+        mma_commit(bar_s_full(x));
+      };
+      auto issue_pv = [&](int x, uint32_t vstage, bool accumulate) {
+        const uint32_t vb = sbase + L::kStage0 + vstage * L::kTileBytes;
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          mma_ts(tO[x], tS[x] + kk * 8, smem_desc_sw128(vb + kk * 2048, 16384, 1024), idesc_pv,
+                 (accumulate || kk > 0) ? 1u : 0u);
+        }
+      };
+      for (int u = blockIdx.x; u < a.num_units && ok; u += gridDim.x) {
+        const UnitInfo ui = unit_info(a, u);
+        if (ui.n_iter == 0) continue;
+        if (!mbar_wait(BAR_Q_FULL, k & 1, abort_flag, a.status, lim)) { ok = false; break; }
+        ++k;
+        tc_fence_after();
+        // prologue: S(0)
+        uint32_t sk = L_cnt % kStages;
+        if (!mbar_wait(bar_kv_full(sk), (L_cnt / kStages) & 1, abort_flag, a.status, lim)) { ok = false; break; }
+        tc_fence_after();
+        for (int x = 0; x < 2; ++x)
+          if (0 >= ui.start[x]) issue_s(x, sk);
+        mma_commit(bar_kv_empty(sk));
+        ++L_cnt;
+        bool first_pv[2] = {a.mode == 0, a.mode == 0};
+        for (int it = 0; it < ui.n_iter; ++it) {
+          const uint32_t sv = L_cnt % kStages;
+          if (!mbar_wait(bar_kv_full(sv), (L_cnt / kStages) & 1, abort_flag, a.status, lim)) { ok = false; break; }
+          ++L_cnt;
+          const bool has_next = it + 1 < ui.n_iter;
+          uint32_t sk2 = 0;
+          if (has_next) {
+            sk2 = L_cnt % kStages;
+            if (!mbar_wait(bar_kv_full(sk2), (L_cnt / kStages) & 1, abort_flag, a.status, lim)) { ok = false; break; }
+            ++L_cnt;
+          }
+          tc_fence_after();
+          for (int x = 0; x < 2 && ok; ++x) {
+            if (it >= ui.start[x]) {
+              if (!mbar_wait(bar_p_full(x), p_cnt[x] & 1, abort_flag, a.status, lim)) { ok = false; break; }
+              ++p_cnt[x];
+              tc_fence_after();
+              issue_pv(x, sv, !first_pv[x]);
+              first_pv[x] = false;
+              if (!has_next) mma_commit(bar_o_full(x));
+            }
+            if (has_next && it + 1 >= ui.start[x]) issue_s(x, sk2);
+          }
+          if (!ok) break;
+          mma_commit(bar_kv_empty(sv));
+          if (has_next) mma_commit(bar_kv_empty(sk2));
+        }
+        if (!ok) break;
+        mma_commit(BAR_Q_EMPTY);
+      }
+      // wait for every MMA issued to finish before TMEM is released
+      mma_commit(BAR_DRAIN);
+      (void)mbar_wait(BAR_DRAIN, 0, abort_flag, nullptr, 100000000ull);
+    }
+  } else {
+    // ------------------------------------------------------------ softmax
+    const int x = (warp - 2) / 4;                 // 0: tile A, 1: tile B
+    const uint32_t quarter = warp & 3;            // TMEM lane quarter of this warp
+    const int r = quarter * 32 + lane;            // row within the tile
+    const uint32_t lane_off = (quarter * 32) << 16;
+    const uint32_t tS = tmem + (x == 0 ? 0u : 128u) + lane_off;
+    const uint32_t tO = tmem + 256u + (x == 0 ? 0u : (uint32_t)D) + lane_off;
+    const float sl2 = a.scale_log2;
+    uint32_t s_cnt = 0, o_cnt = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; u < a.num_units && ok; u += gridDim.x) {
+      const UnitInfo ui = unit_info(a, u);
+      if (ui.start[x] >= ui.n_iter) continue;  // this tile sees no key in this unit
+      const int row = ui.qa_row0 + x * 128 + r;  // tensor row
+      const bool row_ok = row < a.Nq;
+      const long long qpos = ui.qpos0[x] + r;
+      float m_run = -INFINITY, l_run = 0.f;
+      const long long sidx = ((long long)ui.b * a.Hq + ui.h) * a.Nq + row;
+      const long long oidx = (((long long)ui.b * a.Nq + row) * a.Hq + ui.h) * D;
+      if (a.mode == 1) {
+        // load the running state into registers and TMEM
+        if (row_ok) {
+          const float mm = a.m_acc[sidx];
+          m_run = mm == -INFINITY ? -INFINITY : mm * kLog2e;
+          l_run = a.l_acc[sidx];
+        }
+#pragma unroll
+        for (int c = 0; c < D; c += 32) {
+          uint32_t v[32];
+#pragma unroll
+          for (int j = 0; j < 32; j += 4) {
+            float4 f = row_ok ? *reinterpret_cast<const float4*>(a.o_acc + oidx + c + j)
+                              : make_float4(0.f, 0.f, 0.f, 0.f);
+            v[j] = __float_as_uint(f.x);
+            v[j + 1] = __float_as_uint(f.y);
+            v[j + 2] = __float_as_uint(f.z);
+            v[j + 3] = __float_as_uint(f.w);
+          }
+          RA_TMEM_ST32(tO + c, v);
+        }
+      }
+      bool o_valid = (a.mode == 1);  // O_X holds a state that must be rescaled
+      for (int it = ui.start[x]; it < ui.n_iter; ++it) {
+        if (!mbar_wait(bar_s_full(x), s_cnt & 1, abort_flag, a.status, lim)) { ok = false; break; }
+        ++s_cnt;
+        tc_fence_after();
+        const int kt = kt_at(ui, it);
+        uint32_t sr[128];
+#pragma unroll
+        for (int c = 0; c < 128; c += 32) RA_TMEM_LD32(tS + c, (sr + c));
+        tmem_ld_wait();
+        // element masks: causal diagonal tiles and the ragged end of the keys
+        const long long kvpos0 = a.kv_off + (long long)kt * 128;
+        const bool need_mask = (a.causal && kvpos0 + 127 > ui.qpos0[x]) || (kt * 128 + 128 > a.Nkv);
+        if (need_mask) {
+          const long long lim_c = a.causal ? qpos - kvpos0 : 127;  // visible iff c <= lim_c
+          const int nvalid = a.Nkv - kt * 128;
+#pragma unroll
+          for (int c = 0; c < 128; ++c)
+            if (c > lim_c || c >= nvalid) sr[c] = __float_as_uint(-INFINITY);
+        }
+        float mx = __uint_as_float(sr[0]);
+#pragma unroll
+        for (int c = 1; c < 128; ++c) mx = fmaxf(mx, __uint_as_float(sr[c]));
+        const float m_tile = mx * sl2;  // -inf stays -inf (scale > 0)
+        float m_use = m_run;
+        if (m_tile > m_run + kRescaleThreshold) m_use = m_tile;  // also when m_run = -inf
+        const bool rescale = (m_use != m_run);
+        const float alpha = rescale ? ex2_approx(m_run - m_use) : 1.f;  // exp2(-inf) = 0
+        const float neg_m = (m_use == -INFINITY) ? 0.f : -m_use;
+        float rs = 0.f;
+#pragma unroll
+        for (int c = 0; c < 128; c += 32) {
+          uint32_t pk[16];
+#pragma unroll
+          for (int j = 0; j < 32; j += 2) {
+            const float p0 = ex2_approx(fmaf(__uint_as_float(sr[c + j]), sl2, neg_m));
+            const float p1 = ex2_approx(fmaf(__uint_as_float(sr[c + j + 1]), sl2, neg_m));
+            rs += p0 + p1;
+            pk[j / 2] = pack_half2(p0, p1);
+          }
+          RA_TMEM_ST16(tS + c / 2, pk);
+        }
+        l_run = l_run * alpha + rs;
+        m_run = m_use;
+        if (o_valid && __any_sync(0xffffffffu, rescale)) {
+#pragma unroll
+          for (int c = 0; c < D; c += 32) {
+            uint32_t ov[32];
+            RA_TMEM_LD32(tO + c, ov);
+            tmem_ld_wait();
+#pragma unroll
+            for (int j = 0; j < 32; ++j) ov[j] = __float_as_uint(__uint_as_float(ov[j]) * alpha);
+            RA_TMEM_ST32(tO + c, ov);
+          }
+        }
+        o_valid = true;
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(bar_p_full(x));
+      }
+      if (!ok) break;
+      if (!mbar_wait(bar_o_full(x), o_cnt & 1, abort_flag, a.status, lim)) { ok = false; break; }
+      ++o_cnt;
+      tc_fence_after();
+      // epilogue
+      if (a.mode == 0) {
+        const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+        const long long out = ui.b * a.o_bs + ((long long)row * a.Hq + ui.h) * D;
+#pragma unroll
+        for (int c = 0; c < D; c += 32) {
+          uint32_t ov[32];
+          RA_TMEM_LD32(tO + c, ov);
+          tmem_ld_wait();
+          if (row_ok) {
+            if (a.o_dtype == RA_F32) {
+              float* op = static_cast<float*>(a.o_out) + out + c;
+#pragma unroll
+              for (int j = 0; j < 32; j += 4)
+                *reinterpret_cast<float4*>(op + j) =
+                    make_float4(__uint_as_float(ov[j]) * inv, __uint_as_float(ov[j + 1]) * inv,
+                                __uint_as_float(ov[j + 2]) * inv, __uint_as_float(ov[j + 3]) * inv);
+            } else {
+              uint32_t pk[16];
+#pragma unroll
+              for (int j = 0; j < 32; j += 2) {
+                const float f0 = __uint_as_float(ov[j]) * inv, f1 = __uint_as_float(ov[j + 1]) * inv;
+                if (a.o_dtype == RA_BF16) {
+                  __nv_bfloat162 t = __floats2bfloat162_rn(f0, f1);
+                  pk[j / 2] = *reinterpret_cast<uint32_t*>(&t);
+                } else {
+                  pk[j / 2] = pack_half2(f0, f1);
+                }
+              }
+              uint4* op = reinterpret_cast<uint4*>(static_cast<uint16_t*>(a.o_out) + out + c);
+#pragma unroll
+              for (int j = 0; j < 4; ++j) op[j] = make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+            }
+          }
+        }
+        if (row_ok) a.lse[sidx] = l_run > 0.f ? (m_run + log2f(l_run)) * kLn2 : -INFINITY;
+      } else {
+#pragma unroll
+        for (int c = 0; c < D; c += 32) {
+          uint32_t ov[32];
+          RA_TMEM_LD32(tO + c, ov);
+          tmem_ld_wait();
+          if (row_ok) {
+#pragma unroll
+            for (int j = 0; j < 32; j += 4)
+              *reinterpret_cast<float4*>(a.o_acc + oidx + c + j) =
+                  make_float4(__uint_as_float(ov[j]), __uint_as_float(ov[j + 1]),
+                              __uint_as_float(ov[j + 2]), __uint_as_float(ov[j + 3]));
+          }
+        }
+        if (row_ok) {
+          a.m_acc[sidx] = m_run == -INFINITY ? -INFINITY : m_run * kLn2;
+          a.l_acc[sidx] = l_run;
+        }
+      }
+      tc_fence_before();
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem, 512);
+}
+
+}  // namespace
+
+cudaError_t launch_tc_fwd(TcFwdArgs& a, int num_sms, cudaStream_t st) {
+  if (a.num_units <= 0) return cudaSuccess;
+  const int grid = a.num_units < num_sms ? a.num_units : num_sms;
+  cudaError_t e;
+  if (a.d == 128) {
+    e = cudaFuncSetAttribute(tc_fwd_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             FwdSmem<128>::kAlloc);
+    if (e != cudaSuccess) return e;
+    tc_fwd_kernel<128><<<grid, kThreads, FwdSmem<128>::kAlloc, st>>>(a);
+  } else if (a.d == 64) {
+    e = cudaFuncSetAttribute(tc_fwd_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             FwdSmem<64>::kAlloc);
+    if (e != cudaSuccess) return e;
+    tc_fwd_kernel<64><<<grid, kThreads, FwdSmem<64>::kAlloc, st>>>(a);
+  } else {
+    return cudaErrorInvalidValue;
+  }
+  count_launch();
+  return cudaGetLastError();
+}
+
+}  // namespace ra

@@ -1,0 +1,143 @@
+// Internal interface between the C-ABI front end (ra_api.cu) and the kernel
+// translation units.  Not part of the public ABI.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/ra.h"
+
+namespace ra {
+
+// Rows of a [B, N, H, d] tensor: element (b, n, h, c) sits at
+// b * bstride + (n * H + h) * d + c.
+struct Rows {
+  const void* ptr;
+  long long bstride;
+};
+
+// ---------------------------------------------------------------------------
+// fp32 CUDA-core path
+// ---------------------------------------------------------------------------
+struct SimtFwdArgs {
+  const float* q;
+  const float* k;
+  const float* v;
+  int B, Nq, Nkv, Hq, Hkv, d;
+  long long q_bs, kv_bs;
+  float scale;
+  int causal;
+  long long q_off, kv_off;  // block mode: global positions of row 0
+  int P, S;                 // ring mode: P hosts of S rows; P == 0 -> block mode
+  float* o_acc;             // block mode state (read + written)
+  float* m_acc;
+  float* l_acc;
+  void* o_out;              // ring mode outputs
+  int o_dtype;
+  long long o_bs;
+  float* lse;
+};
+
+struct SimtBwdArgs {
+  const float* q;
+  const float* k;
+  const float* v;
+  const float* dO;
+  const float* lse;
+  const float* Dvec;  // [B, Hq, N]
+  int B, N, Hq, Hkv, d;
+  long long q_bs, kv_bs;
+  float scale;
+  int causal;
+  int P, S;
+  void* dq;
+  void* dk;
+  void* dv;
+  int grad_dtype;
+};
+
+cudaError_t launch_simt_fwd(const SimtFwdArgs& a, cudaStream_t st);
+cudaError_t launch_simt_bwd(const SimtBwdArgs& a, cudaStream_t st);
+
+// ---------------------------------------------------------------------------
+// Elementwise / row kernels (any path)
+// ---------------------------------------------------------------------------
+cudaError_t launch_acc_init(float* o, float* m, float* l, int B, int N, int H, int d,
+                            cudaStream_t st);
+cudaError_t launch_merge(float* oa, float* ma, float* la, const float* ob,
+                         const float* mb, const float* lb, int B, int N, int H, int d,
+                         cudaStream_t st);
+cudaError_t launch_finalize(const float* o, const float* m, const float* l, void* out,
+                            int out_dtype, long long out_bs, float* lse, int B, int N,
+                            int H, int d, cudaStream_t st);
+// dst (packed fp16 [B, rows_per_batch]) <- src (dtype, batch stride src_bs);
+// values beyond the fp16 range set RA_ERR_RANGE in *status.
+cudaError_t launch_to_f16(const void* src, int src_dtype, long long src_bs, void* dst,
+                          int B, long long elems_per_batch, int* status,
+                          cudaStream_t st);
+// D[b, h, n] = sum_c dO[b, n, h, c] * O[b, n, h, c]; when lse2 is given also
+// lse2[b, h, n] = lse[b, h, n] * log2(e) (the backward kernel's exponent offset).
+cudaError_t launch_bwd_dot(const void* dO, int do_dtype, const void* o, int o_dtype,
+                           long long q_bs, float* D, const float* lse, float* lse2, int B,
+                           int N, int H, int d, cudaStream_t st);
+// out (dtype, batch stride out_bs) <- mul * src (packed fp32)
+cudaError_t launch_f32_to(const float* src, void* out, int out_dtype, long long out_bs,
+                          int B, long long elems_per_batch, float mul, cudaStream_t st);
+cudaError_t launch_selftest_timeout(unsigned int timeout_us, int* status,
+                                    cudaStream_t st);
+
+// ---------------------------------------------------------------------------
+// tcgen05 tensor-core path (d = 64 or 128, fp16/bf16 operands)
+// ---------------------------------------------------------------------------
+struct TcFwdArgs {
+  // Tensor maps over [B, N, H, d] (dims d, H, N, B), 64-element boxes of 128
+  // rows, 128-byte swizzle.  q/k in qk_dtype, v in fp16.
+  CUtensorMap tm_q, tm_k, tm_v;
+  int qk_bf16;  // 1: q, k are bf16; 0: fp16
+  int B, Nq, Nkv, Hq, Hkv, d;
+  float scale_log2;  // scale * log2(e)
+  int causal;
+  long long q_off, kv_off;
+  int ring_P, ring_S;  // ring mode when ring_P > 0 (Nq == Nkv == P*S, S % 128 == 0)
+  // outputs
+  int mode;         // 0: ring (finalise), 1: block (read/write state)
+  float* o_acc;     // block mode: [B, Nq, Hq, d] fp32
+  float* m_acc;     // [B, Hq, Nq] (natural-log units)
+  float* l_acc;
+  void* o_out;      // ring mode: [B, Nq, Hq, d] in o_dtype, batch stride o_bs
+  int o_dtype;
+  long long o_bs;
+  float* lse;       // [B, Hq, Nq]
+  int* status;
+  unsigned long long wait_limit_ns;
+  int num_units;    // work units (pairs of 128-row query tiles)
+};
+cudaError_t launch_tc_fwd(TcFwdArgs& a, int num_sms, cudaStream_t st);
+
+struct TcBwdArgs {
+  // fp16 operands: q, dO over [B, N, Hq, d]; k, v over [B, N, Hkv, d]
+  CUtensorMap tm_q, tm_k, tm_v, tm_do;
+  int B, N, Hq, Hkv, d;
+  float scale;
+  float scale_log2;
+  int causal;
+  int ring_P, ring_S;
+  const float* lse;   // [B, Hq, N], multiplied by log2(e)
+  const float* Dvec;  // [B, Hq, N]
+  float* dq_acc;      // packed fp32 [B, N, Hq, d], pre-zeroed, reduce-added
+  void* dk;           // [B, N, Hkv, d] in grad_dtype, batch stride kv_bs
+  void* dv;
+  int grad_dtype;
+  long long kv_bs;
+  int* status;
+  unsigned long long wait_limit_ns;
+  int num_units;
+};
+cudaError_t launch_tc_bwd(TcBwdArgs& a, int num_sms, cudaStream_t st);
+
+// Counts kernel launches (ra_launch_count).
+void count_launch(unsigned n = 1);
+
+}  // namespace ra

@@ -1,0 +1,200 @@
+/*
+ * ra.h -- C ABI of the blockwise exact attention library (libra.so), sm_103a.
+ *
+ * Exact softmax attention computed blockwise, as in "Ring Attention with
+ * Blockwise Transformers for Near-Infinite Context" (arXiv 2310.01889,
+ * Abstract: blockwise self-attention over key/value blocks that travel
+ * around a ring of hosts, with no approximation).  On one GPU the ring is
+ * emulated: P virtual hosts own contiguous row blocks of Q, K, V in device
+ * memory and host i computes against key/value block (i - step) mod P at
+ * each step ("Ring Attention: Train 1M Tokens on 8GB GPUs in 2026", section
+ * "Ring Attention: Partition Sequence Length, Not Batch").
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * Layout.  q, k, v, o, dO, dq, dk, dv are [B, N, H, d] with d contiguous and
+ *   heads at stride d (the pages' [seq, heads, head_dim] layout with a batch
+ *   axis; "Building Ring Attention in PyTorch: The 200-Line Version").  The
+ *   batch stride is ra_shape.q_bstride / kv_bstride (elements; 0 means
+ *   packed).  Row blocks of a larger tensor are therefore plain pointer
+ *   offsets.  The fp32 running state is o_acc [B, N_q, Hq, d] (packed) and
+ *   m_acc, l_acc, lse [B, Hq, N_q] (packed).
+ * Scores.  s_ij = scale * q_i . k_j; scale is usually d^-0.5 (same section).
+ *   With causal != 0 key j is visible to query i iff kv_pos(j) <= q_pos(i),
+ *   positions being global row indices (q_off / kv_off added for blocks).
+ * State.  (m, l, o) is the triple the pages carry between ring steps
+ *   (max_score, exp_sum, weighted_output; "Gotchas and Failure Modes"):
+ *   l = sum_j exp(s_j - m), o = sum_j exp(s_j - m) v_j, m in natural-log
+ *   units of the scaled scores.  m is a reference point, not necessarily
+ *   the exact row maximum (kernels may defer rescaling while the maximum
+ *   grows by less than 8 in log2 units); the represented quantities o/l and
+ *   m + log(l) are what the state means.  A row that has seen no key has
+ *   m = -inf, l = 0, o = 0.
+ * Grouped heads.  Hq % Hkv == 0; query head h reads key/value head
+ *   h / (Hq / Hkv).
+ * Streams.  `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *   stream).  Every call only enqueues work and returns; it holds no pointer
+ *   after it returns and allocates no device memory: the caller owns every
+ *   buffer, including the workspace.
+ * Errors.  The return value reports argument validation and launch errors
+ *   (ra_status).  Errors found on the device (a value out of fp16 range in a
+ *   bf16 -> fp16 operand copy, a bounded wait that ran out) are recorded in a
+ *   device status word; ra_sync_status() synchronises the stream and returns
+ *   and clears it.  ra_last_error() gives a message for the last failure on
+ *   the calling thread.
+ * Precision.  RA_F32 inputs run in fp32 CUDA-core arithmetic (exact fp32
+ *   products and sums).  RA_BF16 / RA_F16 inputs with d in {64, 128} run on
+ *   the tcgen05 tensor cores with fp32 accumulation; the probabilities P
+ *   (and dS in the backward pass) are rounded to fp16 for the second
+ *   product, and bf16 operands of those products are copied to fp16 in the
+ *   workspace first (exact for |x| in [2^-14, 65504]; larger values set
+ *   RA_ERR_RANGE in the status word).
+ * Requirements.  Pointers 16-byte aligned; N_q, N_kv, the host block size
+ *   and offsets used with tensor cores multiples of 128 rows for
+ *   ra_ring_fwd / ra_ring_bwd; violations return RA_ERR_INVALID_ARG or
+ *   RA_ERR_UNSUPPORTED.  Nothing falls back to another implementation.
+ */
+#ifndef RA_H_
+#define RA_H_
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum { RA_F32 = 0, RA_BF16 = 1, RA_F16 = 2 } ra_dtype;
+
+typedef enum {
+  RA_OK = 0,
+  RA_ERR_INVALID_ARG = 1, /* bad pointer, size, stride or alignment */
+  RA_ERR_UNSUPPORTED = 2, /* valid but not implemented (e.g. d = 96) */
+  RA_ERR_CUDA = 3,        /* a CUDA runtime/driver call failed */
+  RA_ERR_RANGE = 4,       /* device: operand outside fp16 range */
+  RA_ERR_TIMEOUT = 5      /* device: a bounded wait gave up */
+} ra_status;
+
+typedef struct {
+  int B;                /* batch */
+  int N_q;              /* query rows covered by the call */
+  int N_kv;             /* key/value rows covered by the call */
+  int Hq;               /* query heads */
+  int Hkv;              /* key/value heads (divides Hq) */
+  int d;                /* head dimension */
+  long long q_bstride;  /* elements between batches of q/o/dO/dq; 0 = N_q*Hq*d */
+  long long kv_bstride; /* elements between batches of k/v/dk/dv; 0 = N_kv*Hkv*d */
+} ra_shape;
+
+/* Set the running state to "nothing seen": o_acc = 0, m_acc = -inf,
+ * l_acc = 0 (the ring loop's zero accumulators, "Building Ring Attention in
+ * PyTorch: The 200-Line Version").  Uses shape.B, N_q, Hq, d. */
+int ra_acc_init(float* o_acc, float* m_acc, float* l_acc, ra_shape shape,
+                void* stream);
+
+/* One ring step: fold the scores of a query block against one key/value
+ * block into the running state (o_acc, m_acc, l_acc) with the online-softmax
+ * rescale ("Gotchas and Failure Modes": keep (max, exp_sum,
+ * weighted_output) and rescale on merge; online normaliser of Milakov and
+ * Gimelshein cited by the arXiv 2310.01889 page).
+ *   q      [B, N_q, Hq, d]  query block, global row position q_off + r
+ *   k_blk, v_blk [B, N_kv, Hkv, d]  key/value block at positions kv_off + c
+ *   dtype  type of q, k_blk, v_blk
+ *   o_acc, m_acc, l_acc  state of the query block, read and updated
+ *   causal, scale  as in the conventions above; key/value tiles wholly after
+ *          a query tile are skipped, rows left with no visible key keep
+ *          their state unchanged
+ *   workspace, ws_bytes  at least ra_block_fwd_workspace_bytes(dtype, shape)
+ * Tensor-core dtypes need N_q, N_kv multiples of 128 and d in {64, 128};
+ * RA_F32 accepts any N_q, N_kv >= 1 and d in {32, 64, 128}. */
+int ra_block_fwd(const void* q, const void* k_blk, const void* v_blk,
+                 ra_dtype dtype, float* o_acc, float* m_acc, float* l_acc,
+                 ra_shape shape, long long q_off, long long kv_off, int causal,
+                 float scale, void* workspace, size_t ws_bytes, void* stream);
+size_t ra_block_fwd_workspace_bytes(ra_dtype dtype, ra_shape shape);
+
+/* a <- merge(a, b) for two states of the same query rows: m = max(m_a, m_b),
+ * l = l_a e^{m_a - m} + l_b e^{m_b - m}, o likewise; a side with m = -inf
+ * has weight 0 ("Gotchas and Failure Modes").  Uses shape.B, N_q, Hq, d. */
+int ra_merge(float* o_a, float* m_a, float* l_a, const float* o_b,
+             const float* m_b, const float* l_b, ra_shape shape, void* stream);
+
+/* Final normalisation of the state: O = o / l ("output / softmax_denom" at
+ * the end of the ring loop) written as o_dtype, and lse = m + ln l (natural
+ * log, saved for the backward pass).  Rows with l = 0 give O = 0 and
+ * lse = -inf.  o_out has the q layout of `shape` (q_bstride honoured). */
+int ra_finalize(const float* o_acc, const float* m_acc, const float* l_acc,
+                void* o_out, ra_dtype o_dtype, float* lse, ra_shape shape,
+                void* stream);
+
+/* Whole forward ring in one call: P virtual hosts of S = N/P rows; host i
+ * visits key/value blocks (i - s) mod P for s = 0..P-1, skipping blocks
+ * wholly in its causal future, merges each block into its state and
+ * normalises at the end ("Ring Attention: Partition Sequence Length, Not
+ * Batch"; the loop of "Building Ring Attention in PyTorch: The 200-Line
+ * Version" with the rescaled merge).
+ *   q [B, N, Hq, d], k, v [B, N, Hkv, d] with N = shape.N_q = shape.N_kv
+ *   o [B, N, Hq, d] in o_dtype; lse [B, Hq, N] fp32 (natural log)
+ * Tensor-core dtypes need S a multiple of 128. */
+int ra_ring_fwd(const void* q, const void* k, const void* v, ra_dtype dtype,
+                ra_shape shape, int P, int causal, float scale, void* o,
+                ra_dtype o_dtype, float* lse, void* workspace, size_t ws_bytes,
+                void* stream);
+size_t ra_ring_fwd_workspace_bytes(ra_dtype dtype, ra_shape shape, int P);
+
+/* Backward ring: gradients of L = sum(O * dO).  Probabilities are recomputed
+ * from the saved lse (activation recomputation; "Building Ring Attention in
+ * PyTorch" notes production code needs gradient checkpointing), and the
+ * gradients of each key/value block travel with it around the ring: block
+ * j visits hosts (j + s) mod P ("Gotchas and Failure Modes": gradients flow
+ * backwards through the ring).
+ *   D_i = dO_i . O_i; P_ij = exp(s_ij - lse_i); dV_j = sum_i P_ij dO_i;
+ *   dS_ij = P_ij (dO_i . v_j - D_i); dQ_i = scale sum_j dS_ij k_j;
+ *   dK_j = scale sum_i dS_ij q_i (summed over the query heads of a group).
+ *   o in o_dtype, dO in dtype, lse from ra_ring_fwd; dq [B,N,Hq,d],
+ *   dk, dv [B,N,Hkv,d] written in grad_dtype (fully overwritten). */
+int ra_ring_bwd(const void* q, const void* k, const void* v, const void* o,
+                ra_dtype o_dtype, const void* dO, const float* lse,
+                ra_dtype dtype, ra_shape shape, int P, int causal, float scale,
+                void* dq, void* dk, void* dv, ra_dtype grad_dtype,
+                void* workspace, size_t ws_bytes, void* stream);
+size_t ra_ring_bwd_workspace_bytes(ra_dtype dtype, ra_dtype grad_dtype,
+                                   ra_shape shape, int P);
+
+/* Synchronise `stream`, then return and clear the device status word
+ * (RA_OK, RA_ERR_RANGE or RA_ERR_TIMEOUT), or RA_ERR_CUDA if the stream
+ * itself reports an error. */
+int ra_sync_status(void* stream);
+
+/* Message for the last non-OK return on the calling thread ("" if none). */
+const char* ra_last_error(void);
+
+/* Number of kernels this library has launched in this process. */
+unsigned long long ra_launch_count(void);
+
+/* Kernel timing.  While enabled, every launch of the kernels below is
+ * bracketed by CUDA events recorded on the stream it is launched on;
+ * ra_kernel_timing_read() waits for those events and returns the summed
+ * device time (ms) and the number of launches since timing was enabled.
+ * ra_kernel_timing(1) enables and resets, ra_kernel_timing(0) disables and
+ * releases the events.  Used by the benchmark to time the dominant kernel. */
+typedef enum {
+  RA_KERNEL_FWD_TC = 0,   /* tensor-core forward (ring and block step) */
+  RA_KERNEL_BWD_TC = 1,   /* tensor-core backward */
+  RA_KERNEL_FWD_F32 = 2,  /* fp32 CUDA-core forward */
+  RA_KERNEL_BWD_F32 = 3,  /* fp32 CUDA-core backward (both kernels) */
+  RA_KERNEL_COUNT = 4
+} ra_kernel_id;
+int ra_kernel_timing(int enable);
+int ra_kernel_timing_read(int kernel, double* total_ms, unsigned long long* launches);
+
+/* Self-test of the bounded wait: launches one CTA that waits on an mbarrier
+ * nobody arrives at, with a limit of timeout_us microseconds; the kernel must
+ * give up, record RA_ERR_TIMEOUT in the status word and return.  Returns the
+ * launch status; read the outcome with ra_sync_status(). */
+int ra_selftest_timeout(unsigned int timeout_us, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* RA_H_ */

@@ -1,0 +1,89 @@
+"""CPU-only checks of the C ABI: the library loads, exports every symbol the
+header declares, and rejects bad arguments before touching a GPU."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "ra.h")
+
+
+@pytest.fixture(scope="module")
+def ra():
+    import __graft_entry__
+    __graft_entry__.build()
+    import blockwise_exact_attention_ra_gb300 as ra
+    return ra
+
+
+def declared_symbols():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(ra_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_header_declares_the_entry_points():
+    syms = declared_symbols()
+    for need in ("ra_block_fwd", "ra_merge", "ra_ring_fwd", "ra_ring_bwd", "ra_finalize",
+                 "ra_acc_init", "ra_sync_status", "ra_last_error"):
+        assert need in syms
+
+
+def test_library_exports_every_declared_symbol(ra):
+    lib = ctypes.CDLL(ra._LIBPATH)
+    for s in declared_symbols():
+        assert hasattr(lib, s), s
+        assert hasattr(ra, s), f"binding lacks {s}"
+
+
+def test_workspace_sizes(ra):
+    sh = ra.RaShape(1, 1024, 1024, 4, 2, 128, 0, 0)
+    assert ra.ra_ring_fwd_workspace_bytes(ra.RA_BF16, sh, 4) >= 1024 * 2 * 128 * 2
+    assert ra.ra_ring_fwd_workspace_bytes(ra.RA_F16, sh, 4) == 0
+    assert ra.ra_ring_fwd_workspace_bytes(ra.RA_F32, sh, 4) == 0
+    ws = ra.ra_ring_bwd_workspace_bytes(ra.RA_BF16, ra.RA_F32, sh, 4)
+    # D, LSE*log2e, fp32 dq accumulator, fp16 copies of q, k, v, dO
+    need = 2 * 4 * 1024 * 4 + 1024 * 4 * 128 * 4 + 2 * (1024 * 4 * 128 * 2) + 2 * (1024 * 2 * 128 * 2)
+    assert ws >= need
+    assert ra.ra_ring_bwd_workspace_bytes(ra.RA_F32, ra.RA_F32, sh, 4) == 4 * 1024 * 4
+    assert ra.ra_block_fwd_workspace_bytes(ra.RA_BF16, sh) >= 1024 * 2 * 128 * 2
+
+
+def test_bad_shapes_are_rejected_without_a_gpu(ra):
+    lib = ra.lib
+    vp = ctypes.c_void_p(16)
+    for sh in (ra.RaShape(0, 128, 128, 1, 1, 64, 0, 0),      # B = 0
+               ra.RaShape(1, 128, 128, 3, 2, 64, 0, 0),      # Hq % Hkv != 0
+               ra.RaShape(1, 128, 128, 2, 2, 0, 0, 0),       # d = 0
+               ra.RaShape(1, 128, 128, 2, 2, 64, 5, 0)):     # batch stride < one batch
+        rc = lib.ra_ring_fwd(vp, vp, vp, ra.RA_BF16, sh, 1, 1, 0.1, vp, ra.RA_F32, vp, None, 0, None)
+        assert rc == 1, (sh.B, sh.Hq, sh.Hkv, sh.d)
+        assert ra.ra_last_error()
+    ok = ra.RaShape(1, 512, 512, 2, 2, 64, 0, 0)
+    assert lib.ra_ring_fwd(vp, vp, vp, 7, ok, 1, 1, 0.1, vp, ra.RA_F32, vp, None, 0, None) == 1   # dtype
+    assert lib.ra_ring_fwd(vp, vp, vp, ra.RA_BF16, ok, 3, 1, 0.1, vp, ra.RA_F32, vp, None, 0, None) == 1  # P
+    assert lib.ra_ring_fwd(vp, vp, vp, ra.RA_BF16, ok, 1, 1, -1.0, vp, ra.RA_F32, vp, None, 0, None) == 1  # scale
+    assert lib.ra_ring_fwd(vp, vp, vp, ra.RA_BF16, ok, 1, 1, float("nan"), vp, ra.RA_F32, vp, None, 0, None) == 1
+    neq = ra.RaShape(1, 512, 256, 2, 2, 64, 0, 0)
+    assert lib.ra_ring_fwd(vp, vp, vp, ra.RA_BF16, neq, 1, 1, 0.1, vp, ra.RA_F32, vp, None, 0, None) == 1
+    odd = ra.RaShape(1, 384, 384, 2, 2, 64, 0, 0)   # host block 192 is not a multiple of 128
+    assert lib.ra_ring_fwd(vp, vp, vp, ra.RA_BF16, odd, 2, 1, 0.1, vp, ra.RA_F32, vp, None, 0, None) == 2
+
+
+def test_null_and_misaligned_pointers_are_rejected(ra):
+    lib = ra.lib
+    sh = ra.RaShape(1, 512, 512, 2, 2, 64, 0, 0)
+    vp = ctypes.c_void_p(256)
+    assert lib.ra_ring_fwd(None, vp, vp, ra.RA_BF16, sh, 1, 1, 0.1, vp, ra.RA_F32, vp, None, 0, None) == 1
+    assert "q" in ra.ra_last_error()
+    bad = ctypes.c_void_p(258)
+    assert lib.ra_ring_fwd(vp, bad, vp, ra.RA_BF16, sh, 1, 1, 0.1, vp, ra.RA_F32, vp, None, 0, None) == 1
+    assert "aligned" in ra.ra_last_error()
+    assert lib.ra_merge(vp, vp, None, vp, vp, vp, sh, None) == 1
+    assert lib.ra_block_fwd(vp, vp, vp, ra.RA_BF16, vp, vp, vp, sh, -1, 0, 1, 0.1, None, 0, None) == 1
+
+
+def test_launch_counter_is_readable(ra):
+    assert isinstance(ra.ra_launch_count(), int) and ra.ra_launch_count() >= 0
