@@ -1,0 +1,388 @@
+#!/usr/bin/env python
+"""Benchmark: causal bf16 ring attention, forward + backward, N = 131072,
+16 heads, d = 128, P = 32 virtual hosts, on one GB300 per process.
+
+One step = ra_ring_fwd + ra_ring_bwd over the whole sequence (every row of
+the hot path).  Inputs are seeded synthetic tensors resident in HBM (each of
+Q, K, V, dO is 512 MiB, larger than L2, so no flush is needed between steps).
+Prints one JSON line (rank 0).  With --impl reference the fp64 CPU oracle is
+timed on a bounded sample of the same workload instead.
+
+Multi-GPU: the workload does not exchange data between GPUs (the ring is
+emulated inside one GPU), so N processes run N independent replicas; the
+step time is the maximum over ranks and the value sums the work of all ranks.
+"""
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "causal attention TFLOP/s fwd+bwd at 128K bf16 d=128; % of GB300 BF16 peak"
+WORKLOAD = dict(B=1, N=131072, Hq=16, Hkv=16, d=128, P=32, causal=True, cid=3)
+WORKLOAD_NAME = "bf16 causal ring attention fwd+bwd, B1 H16 N131072 d128, P32 virtual hosts of 4096"
+
+
+def algo_flops(B, N, Hq, d, causal=True):
+    """Causal-adjusted algorithmic flops: fwd 4*B*H*N^2*d/2 (two products of
+    2*N*N*d over the visible half), bwd 2.5x fwd (five products, two of them
+    shared with the forward)."""
+    fwd = 4.0 * B * Hq * N * N * d / (2.0 if causal else 1.0)
+    return fwd, 2.5 * fwd
+
+
+def row_flops(i, d, causal=True, N=None):
+    """Algorithmic flops of one query row in fwd+bwd: 14 * d * (keys seen)."""
+    keys = (i + 1) if causal else N
+    return 4.0 * d * keys * 3.5
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return dict(burst=float(p["bf16_tflops"]), sustained=float(p["bf16_tflops_sustained"]),
+                    hbm=float(p["hbm_gbs"]), source="measured (MEASURED_PEAKS.json)")
+    except Exception:
+        return dict(burst=1900.0, sustained=1700.0, hbm=6800.0, source="fallback")
+
+
+def kernel_traffic(kernel):
+    """DRAM bytes per launch from the committed ncu summary, only if it was
+    taken on the current kernel source (sha256 of the .cu file)."""
+    import hashlib
+    src = {"tc_bwd": "ra_bwd_tc.cu", "tc_fwd": "ra_fwd_tc.cu"}[kernel]
+    path = os.path.join(ROOT, "blockwise_exact_attention_ra_gb300", "csrc", src)
+    sha = hashlib.sha256(open(path, "rb").read()).hexdigest()[:16]
+    table = os.path.join(ROOT, "profiles", "dram_traffic.txt")
+    if not os.path.exists(table):
+        return None
+    for line in open(table):
+        parts = line.split()
+        if len(parts) >= 3 and not line.startswith("#") and parts[0] == kernel and parts[1] == sha:
+            return float(parts[2])
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi samples every 200 ms while the timed region runs."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    NAMES = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+
+    def __init__(self, device_index):
+        self.dev = device_index
+        self.proc = None
+        self.file = None
+
+    def start(self):
+        try:
+            self.file = tempfile.TemporaryFile(mode="w+")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200", "-i", str(self.dev)], stdout=self.file, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.file.seek(0)
+        sm, mx, reasons = [], [], set()
+        for line in self.file:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, val in zip(self.NAMES, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def cpu_oracle_sample(q, k, v, do, rows, causal, scale):
+    """Run the oracle (fwd + bwd incl. dK/dV contributions) on `rows`; returns
+    (seconds, algorithmic flops of those rows)."""
+    import oracle
+    heads = sorted({h for _, h, _ in rows})
+    hk = {}
+    for h in heads:
+        hk[h] = tuple(t[:, :, h:h + 1].float().cpu().numpy().astype(np.float64) for t in (q, k, v, do))
+    t0 = time.perf_counter()
+    for h in heads:
+        qq, kk, vv, dd = hk[h]
+        sel = [(b, 0, i) for b, hh, i in rows if hh == h]
+        oracle.attention_rows(qq, kk, vv, sel, causal, scale, do=dd, want_kv_grads=True)
+    dt = time.perf_counter() - t0
+    N = q.shape[1]
+    fl = sum(row_flops(i, q.shape[3], causal, N) for _, _, i in rows)
+    return dt, fl
+
+
+def oracle_threads():
+    try:
+        import threadpoolctl
+        info = threadpoolctl.threadpool_info()
+        n = [x.get("num_threads") for x in info if x.get("user_api") == "blas"]
+        if n:
+            return int(max(n))
+    except Exception:
+        pass
+    return os.cpu_count()
+
+
+def sample_rows(N, Hq, count, seed):
+    g = torch.Generator().manual_seed(seed)
+    h = int(torch.randint(Hq, (1,), generator=g))
+    idx = torch.randint(N, (count,), generator=g)
+    return [(0, h, int(i)) for i in idx]
+
+
+def run_reference(args, ws, rank):
+    """Reference arm: the fp64 oracle on the host cores, bounded row samples."""
+    if rank != 0:
+        return
+    from blockwise_exact_attention_ra_gb300.inputs import make_tensors
+    W = WORKLOAD
+    q, k, v, do = make_tensors(W["B"], W["N"], W["Hq"], W["Hkv"], W["d"], torch.bfloat16, "cpu",
+                               1000 + W["cid"], with_do=True)
+    scale = W["d"] ** -0.5
+    times, flops = [], []
+    for s in range(args.warmup + args.steps):
+        rows = sample_rows(W["N"], W["Hq"], args.ref_rows, 500 + s)
+        dt, fl = cpu_oracle_sample(q, k, v, do, rows, True, scale)
+        if s >= args.warmup:
+            times.append(dt)
+            flops.append(fl)
+    value = sum(flops) / sum(times) / 1e12
+    cores = oracle_threads()
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * sum(times) / len(times),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": WORKLOAD_NAME, "B": W["B"], "N": W["N"], "Hq": W["Hq"], "Hkv": W["Hkv"],
+                   "d": W["d"], "P": W["P"], "causal": True, "parallelism": "replicas"},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                         "sample": f"{args.ref_rows} seeded query rows of one head per step, fwd+bwd "
+                                   f"(incl. their dK/dV contributions), fp64 numpy"},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args, ws, rank, local):
+    import blockwise_exact_attention_ra_gb300 as ra
+    from blockwise_exact_attention_ra_gb300.inputs import make_tensors
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    W = WORKLOAD
+    B, N, Hq, Hkv, d, P = W["B"], W["N"], W["Hq"], W["Hkv"], W["d"], W["P"]
+    scale = d ** -0.5
+    q, k, v, do = make_tensors(B, N, Hq, Hkv, d, torch.bfloat16, dev, 1000 + W["cid"] + 17 * rank)
+    o = torch.empty(B, N, Hq, d, dtype=torch.float32, device=dev)
+    lse = torch.empty(B, Hq, N, dtype=torch.float32, device=dev)
+    dq = torch.empty(B, N, Hq, d, dtype=torch.float32, device=dev)
+    dk = torch.empty(B, N, Hkv, d, dtype=torch.float32, device=dev)
+    dv = torch.empty(B, N, Hkv, d, dtype=torch.float32, device=dev)
+    sh = ra.shape_of(q, k)
+    wsf = torch.empty(max(16, ra.ra_ring_fwd_workspace_bytes(ra.RA_BF16, sh, P)), dtype=torch.uint8, device=dev)
+    wsb = torch.empty(max(16, ra.ra_ring_bwd_workspace_bytes(ra.RA_BF16, ra.RA_F32, sh, P)),
+                      dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(ev=None):
+        ra.ra_ring_fwd(q, k, v, P, True, scale, o, lse, wsf, stream)
+        if ev is not None:
+            ev.record(stream)
+        ra.ra_ring_bwd(q, k, v, o, do, lse, P, True, scale, dq, dk, dv, wsb, stream)
+
+    for _ in range(args.warmup):
+        step()
+    ra.ra_sync_status(stream)
+
+    fwd_fl, bwd_fl = algo_flops(B, N, Hq, d)
+    n_ev = args.steps
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(n_ev)]
+    mids = [torch.cuda.Event(enable_timing=True) for _ in range(n_ev)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(n_ev)]
+    clocks = ClockSampler(local)
+    launches0 = ra.ra_launch_count()
+    ra.ra_kernel_timing(1)
+    if ws > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize(dev)
+    clocks.start()
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for s in range(args.steps):
+        starts[s].record(stream)
+        step(mids[s])
+        ends[s].record(stream)
+    t_end.record(stream)
+    torch.cuda.synchronize(dev)
+    clk = clocks.stop()
+    if ws > 1:
+        torch.distributed.barrier()
+    ra.ra_sync_status(stream)
+    launches = ra.ra_launch_count() - launches0
+    total_ms = t_start.elapsed_time(t_end)
+    fwd_ms = sum(s.elapsed_time(m) for s, m in zip(starts, mids)) / args.steps
+    bwd_ms = sum(m.elapsed_time(e) for m, e in zip(mids, ends)) / args.steps
+    ktime = {kid: ra.ra_kernel_timing_read(kid) for kid in (ra.RA_KERNEL_FWD_TC, ra.RA_KERNEL_BWD_TC)}
+    ra.ra_kernel_timing(0)
+
+    ms_step = total_ms / args.steps
+    if ws > 1:
+        t = torch.tensor([ms_step], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms_step = float(t.item())
+    value = ws * (fwd_fl + bwd_fl) / (ms_step * 1e-3) / 1e12
+    peaks = load_peaks()
+
+    # dominant kernel: the one with the larger share of device time
+    fwd_k_ms, fwd_n = ktime[ra.RA_KERNEL_FWD_TC]
+    bwd_k_ms, bwd_n = ktime[ra.RA_KERNEL_BWD_TC]
+    kern = {
+        "tc_fwd": {"avg_ms": fwd_k_ms / max(fwd_n, 1), "launches": fwd_n, "flop_per_launch": fwd_fl},
+        "tc_bwd": {"avg_ms": bwd_k_ms / max(bwd_n, 1), "launches": bwd_n, "flop_per_launch": bwd_fl},
+    }
+    for kk in kern.values():
+        kk["tflops"] = kk["flop_per_launch"] / (kk["avg_ms"] * 1e-3) / 1e12
+        kk["frac_of_peak"] = kk["tflops"] / peaks["sustained"]
+    dom = "tc_bwd" if bwd_k_ms >= fwd_k_ms else "tc_fwd"
+    roof = {"bound": "tensor", "kernel": dom, "achieved": kern[dom]["tflops"], "peak": peaks["sustained"],
+            "unit": "TFLOP/s", "frac": kern[dom]["tflops"] / peaks["sustained"],
+            "traffic": kernel_traffic(dom),
+            "peak_source": peaks["source"] + ", bf16 sustained (dense fp16 runs at the bf16 rate)"}
+
+    # end to end through the public API with pinned host buffers
+    e2e = None
+    if not args.no_e2e:
+        hq = [t.to("cpu").pin_memory() for t in (q, k, v, do)]
+        dq_ = [torch.empty_like(t) for t in (q, k, v, do)]
+        o16 = torch.empty(B, N, Hq, d, dtype=torch.bfloat16, device=dev)
+        g16 = [torch.empty(B, N, Hq, d, dtype=torch.bfloat16, device=dev),
+               torch.empty(B, N, Hkv, d, dtype=torch.bfloat16, device=dev),
+               torch.empty(B, N, Hkv, d, dtype=torch.bfloat16, device=dev)]
+        wsb16 = torch.empty(max(16, ra.ra_ring_bwd_workspace_bytes(ra.RA_BF16, ra.RA_BF16, sh, P)),
+                            dtype=torch.uint8, device=dev)
+        host_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in [o16] + g16]
+
+        def e2e_step():
+            for h, dd in zip(hq, dq_):
+                dd.copy_(h, non_blocking=True)
+            ra.ra_ring_fwd(dq_[0], dq_[1], dq_[2], P, True, scale, o16, lse, wsf, stream)
+            ra.ra_ring_bwd(dq_[0], dq_[1], dq_[2], o16, dq_[3], lse, P, True, scale, g16[0], g16[1], g16[2],
+                           wsb16, stream)
+            for dst, src in zip(host_out, [o16] + g16):
+                dst.copy_(src, non_blocking=True)
+
+        for _ in range(max(1, args.warmup)):
+            e2e_step()
+        torch.cuda.synchronize(dev)
+        if ws > 1:
+            torch.distributed.barrier()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(args.steps):
+            e2e_step()
+        b.record(stream)
+        torch.cuda.synchronize(dev)
+        ra.ra_sync_status(stream)
+        e_ms = a.elapsed_time(b) / args.steps
+        if ws > 1:
+            t = torch.tensor([e_ms], device=dev)
+            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+            e_ms = float(t.item())
+        e2e = {"value": ws * (fwd_fl + bwd_fl) / (e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+               "ms_per_step": e_ms,
+               "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in hq),
+               "d2h_bytes_per_step": sum(t.numel() * t.element_size() for t in host_out)}
+
+    cpu = None
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        rows = sample_rows(N, Hq, args.cpu_rows, 4242)
+        dt, fl = cpu_oracle_sample(q, k, v, do, rows, True, scale)
+        cpu = {"value": fl / dt / 1e12, "unit": "TFLOP/s", "cores": oracle_threads(), "kind": "oracle",
+               "sample": f"{args.cpu_rows} seeded query rows of one head, fwd+bwd incl. their dK/dV "
+                         f"contributions, fp64 numpy; {dt:.1f} s"}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": ws, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": WORKLOAD_NAME, "B": B, "N": N, "Hq": Hq, "Hkv": Hkv, "d": d, "P": P,
+                       "causal": True, "l2": "inputs larger than L2 (Q, K, V, dO 512 MiB each); no flush",
+                       "parallelism": "replicas" if ws > 1 else "single GPU"},
+            "pct_of_peak": value / ws / peaks["sustained"],
+            "fwd_ms": fwd_ms, "bwd_ms": bwd_ms,
+            "fwd_tflops": fwd_fl / (fwd_ms * 1e-3) / 1e12, "bwd_tflops": bwd_fl / (bwd_ms * 1e-3) / 1e12,
+            "kernels": kern, "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
+            "gpu_launches": launches, "clocks": clk,
+        }
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        torch.distributed.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-rows", type=int, default=3072)
+    ap.add_argument("--ref-rows", type=int, default=48)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    ws, rank, local = dist_env()
+    if args.impl == "reference":
+        run_reference(args, ws, rank)
+    else:
+        run_ours(args, ws, rank, local)
+
+
+if __name__ == "__main__":
+    main()

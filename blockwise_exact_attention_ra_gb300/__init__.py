@@ -22,9 +22,11 @@ __all__ = [
     "ra_sync_status", "ra_last_error", "ra_launch_count", "ra_selftest_timeout",
     "ra_kernel_timing", "ra_kernel_timing_read",
     "ring_attention_fwd", "ring_attention_bwd", "RA_F32", "RA_BF16", "RA_F16",
+    "RA_CAUSAL", "RA_PRECISE",
 ]
 
 RA_F32, RA_BF16, RA_F16 = 0, 1, 2
+RA_CAUSAL, RA_PRECISE = 1, 2
 STATUS = {0: "RA_OK", 1: "RA_ERR_INVALID_ARG", 2: "RA_ERR_UNSUPPORTED", 3: "RA_ERR_CUDA",
           4: "RA_ERR_RANGE", 5: "RA_ERR_TIMEOUT"}
 _DTYPES = {torch.float32: RA_F32, torch.bfloat16: RA_BF16, torch.float16: RA_F16}
@@ -166,13 +168,13 @@ def ra_block_fwd_workspace_bytes(dtype, shape):
 
 
 def ra_block_fwd(q, k_blk, v_blk, o_acc, m_acc, l_acc, q_off, kv_off, causal, scale,
-                 workspace=None, shape=None, stream=None):
+                 workspace=None, shape=None, stream=None, precise=False):
     """Fold one key/value block into the running state of a query block."""
     shape = shape or shape_of(q, k_blk)
     dt = _dt(q)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _check(lib.ra_block_fwd(_ptr(q), _ptr(k_blk), _ptr(v_blk), dt, _ptr(o_acc), _ptr(m_acc),
-                            _ptr(l_acc), shape, int(q_off), int(kv_off), int(bool(causal)),
+                            _ptr(l_acc), shape, int(q_off), int(kv_off), _flags(causal, precise),
                             float(scale), _ptr(workspace), ws_bytes, _stream(stream)))
 
 
@@ -190,10 +192,10 @@ def ra_ring_fwd_workspace_bytes(dtype, shape, P):
     return int(lib.ra_ring_fwd_workspace_bytes(dtype, shape, P))
 
 
-def ra_ring_fwd(q, k, v, P, causal, scale, o, lse, workspace=None, stream=None):
+def ra_ring_fwd(q, k, v, P, causal, scale, o, lse, workspace=None, stream=None, precise=False):
     shape = shape_of(q, k)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
-    _check(lib.ra_ring_fwd(_ptr(q), _ptr(k), _ptr(v), _dt(q), shape, int(P), int(bool(causal)),
+    _check(lib.ra_ring_fwd(_ptr(q), _ptr(k), _ptr(v), _dt(q), shape, int(P), _flags(causal, precise),
                            float(scale), _ptr(o), _dt(o), _ptr(lse), _ptr(workspace), ws_bytes,
                            _stream(stream)))
 
@@ -202,13 +204,18 @@ def ra_ring_bwd_workspace_bytes(dtype, grad_dtype, shape, P):
     return int(lib.ra_ring_bwd_workspace_bytes(dtype, grad_dtype, shape, P))
 
 
-def ra_ring_bwd(q, k, v, o, dO, lse, P, causal, scale, dq, dk, dv, workspace, stream=None):
+def ra_ring_bwd(q, k, v, o, dO, lse, P, causal, scale, dq, dk, dv, workspace, stream=None,
+                precise=False):
     shape = shape_of(q, k)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _check(lib.ra_ring_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _dt(o), _ptr(dO), _ptr(lse),
-                           _dt(q), shape, int(P), int(bool(causal)), float(scale), _ptr(dq),
+                           _dt(q), shape, int(P), _flags(causal, precise), float(scale), _ptr(dq),
                            _ptr(dk), _ptr(dv), _dt(dq), _ptr(workspace), ws_bytes,
                            _stream(stream)))
+
+
+def _flags(causal, precise):
+    return (RA_CAUSAL if causal else 0) | (RA_PRECISE if precise else 0)
 
 
 def _workspace(nbytes, device):
@@ -216,7 +223,7 @@ def _workspace(nbytes, device):
 
 
 def ring_attention_fwd(q, k, v, P, causal=True, scale=None, o_dtype=torch.float32,
-                       stream=None):
+                       stream=None, precise=False):
     """Allocate O [B,N,Hq,d] (o_dtype) and LSE [B,Hq,N] fp32 and run the ring forward."""
     if scale is None:
         scale = q.shape[-1] ** -0.5
@@ -224,12 +231,12 @@ def ring_attention_fwd(q, k, v, P, causal=True, scale=None, o_dtype=torch.float3
     o = torch.empty(B, N, Hq, d, dtype=o_dtype, device=q.device)
     lse = torch.empty(B, Hq, N, dtype=torch.float32, device=q.device)
     ws = _workspace(ra_ring_fwd_workspace_bytes(_dt(q), shape_of(q, k), P), q.device)
-    ra_ring_fwd(q, k, v, P, causal, scale, o, lse, ws, stream)
+    ra_ring_fwd(q, k, v, P, causal, scale, o, lse, ws, stream, precise)
     return o, lse
 
 
 def ring_attention_bwd(q, k, v, o, lse, dO, P, causal=True, scale=None,
-                       grad_dtype=torch.float32, stream=None):
+                       grad_dtype=torch.float32, stream=None, precise=False):
     """Allocate dQ, dK, dV (grad_dtype) and workspace and run the ring backward."""
     if scale is None:
         scale = q.shape[-1] ** -0.5
@@ -238,5 +245,5 @@ def ring_attention_bwd(q, k, v, o, lse, dO, P, causal=True, scale=None,
     dv = torch.empty(v.shape, dtype=grad_dtype, device=q.device)
     ws = _workspace(ra_ring_bwd_workspace_bytes(_dt(q), _DTYPES[grad_dtype], shape_of(q, k), P),
                     q.device)
-    ra_ring_bwd(q, k, v, o, dO, lse, P, causal, scale, dq, dk, dv, ws, stream)
+    ra_ring_bwd(q, k, v, o, dO, lse, P, causal, scale, dq, dk, dv, ws, stream, precise)
     return dq, dk, dv

@@ -367,8 +367,10 @@ size_t ra_block_fwd_workspace_bytes(ra_dtype dtype, ra_shape shape) {
 
 int ra_block_fwd(const void* q, const void* k_blk, const void* v_blk, ra_dtype dtype,
                  float* o_acc, float* m_acc, float* l_acc, ra_shape shape, long long q_off,
-                 long long kv_off, int causal, float scale, void* workspace, size_t ws_bytes,
+                 long long kv_off, int flags, float scale, void* workspace, size_t ws_bytes,
                  void* stream) {
+  const int causal = (flags & RA_CAUSAL) != 0, precise = (flags & RA_PRECISE) != 0;
+  if (flags & ~(RA_CAUSAL | RA_PRECISE)) return fail(RA_ERR_INVALID_ARG, "unknown flag bits 0x%x", flags);
   Shape s;
   int rc;
   if ((rc = check_shape(shape, &s))) return rc;
@@ -390,7 +392,7 @@ int ra_block_fwd(const void* q, const void* k_blk, const void* v_blk, ra_dtype d
     a.v = static_cast<const float*>(v_blk);
     a.B = s.B; a.Nq = s.Nq; a.Nkv = s.Nkv; a.Hq = s.Hq; a.Hkv = s.Hkv; a.d = s.d;
     a.q_bs = s.q_bs; a.kv_bs = s.kv_bs;
-    a.scale = scale; a.causal = causal != 0; a.q_off = q_off; a.kv_off = kv_off;
+    a.scale = scale; a.causal = causal; a.q_off = q_off; a.kv_off = kv_off;
     a.P = 0; a.S = 0;
     a.o_acc = o_acc; a.m_acc = m_acc; a.l_acc = l_acc;
     TimedLaunch tl(RA_KERNEL_FWD_F32, cs);
@@ -420,7 +422,7 @@ int ra_block_fwd(const void* q, const void* k_blk, const void* v_blk, ra_dtype d
   a.qk_bf16 = bf;
   a.B = s.B; a.Nq = s.Nq; a.Nkv = s.Nkv; a.Hq = s.Hq; a.Hkv = s.Hkv; a.d = s.d;
   a.scale_log2 = scale * 1.4426950408889634f;
-  a.causal = causal != 0; a.q_off = q_off; a.kv_off = kv_off;
+  a.causal = causal; a.q_off = q_off; a.kv_off = kv_off; a.precise = precise;
   a.ring_P = 0; a.ring_S = 0; a.mode = 1;
   a.o_acc = o_acc; a.m_acc = m_acc; a.l_acc = l_acc;
   a.status = st;
@@ -448,8 +450,10 @@ static int check_ring(const Shape& s, int P, int dtype) {
 }
 
 int ra_ring_fwd(const void* q, const void* k, const void* v, ra_dtype dtype, ra_shape shape,
-                int P, int causal, float scale, void* o, ra_dtype o_dtype, float* lse,
+                int P, int flags, float scale, void* o, ra_dtype o_dtype, float* lse,
                 void* workspace, size_t ws_bytes, void* stream) {
+  const int causal = (flags & RA_CAUSAL) != 0, precise = (flags & RA_PRECISE) != 0;
+  if (flags & ~(RA_CAUSAL | RA_PRECISE)) return fail(RA_ERR_INVALID_ARG, "unknown flag bits 0x%x", flags);
   Shape s;
   int rc;
   if ((rc = check_shape(shape, &s))) return rc;
@@ -471,7 +475,7 @@ int ra_ring_fwd(const void* q, const void* k, const void* v, ra_dtype dtype, ra_
     a.v = static_cast<const float*>(v);
     a.B = s.B; a.Nq = s.Nq; a.Nkv = s.Nkv; a.Hq = s.Hq; a.Hkv = s.Hkv; a.d = s.d;
     a.q_bs = s.q_bs; a.kv_bs = s.kv_bs;
-    a.scale = scale; a.causal = causal != 0;
+    a.scale = scale; a.causal = causal;
     a.P = P; a.S = s.Nq / P;
     a.o_out = o; a.o_dtype = o_dtype; a.o_bs = s.q_bs; a.lse = lse;
     TimedLaunch tl(RA_KERNEL_FWD_F32, cs);
@@ -501,8 +505,8 @@ int ra_ring_fwd(const void* q, const void* k, const void* v, ra_dtype dtype, ra_
   a.qk_bf16 = bf;
   a.B = s.B; a.Nq = s.Nq; a.Nkv = s.Nkv; a.Hq = s.Hq; a.Hkv = s.Hkv; a.d = s.d;
   a.scale_log2 = scale * 1.4426950408889634f;
-  a.causal = causal != 0;
-  a.ring_P = P; a.ring_S = s.Nq / P; a.mode = 0;
+  a.causal = causal;
+  a.ring_P = P; a.ring_S = s.Nq / P; a.mode = 0; a.precise = precise;
   a.o_out = o; a.o_dtype = o_dtype; a.o_bs = s.q_bs; a.lse = lse;
   a.status = st;
   a.wait_limit_ns = wait_limit_ns();
@@ -547,8 +551,10 @@ size_t ra_ring_bwd_workspace_bytes(ra_dtype dtype, ra_dtype grad_dtype, ra_shape
 
 int ra_ring_bwd(const void* q, const void* k, const void* v, const void* o, ra_dtype o_dtype,
                 const void* dO, const float* lse, ra_dtype dtype, ra_shape shape, int P,
-                int causal, float scale, void* dq, void* dk, void* dv, ra_dtype grad_dtype,
+                int flags, float scale, void* dq, void* dk, void* dv, ra_dtype grad_dtype,
                 void* workspace, size_t ws_bytes, void* stream) {
+  const int causal = (flags & RA_CAUSAL) != 0, precise = (flags & RA_PRECISE) != 0;
+  if (flags & ~(RA_CAUSAL | RA_PRECISE)) return fail(RA_ERR_INVALID_ARG, "unknown flag bits 0x%x", flags);
   Shape s;
   int rc;
   if ((rc = check_shape(shape, &s))) return rc;
@@ -584,7 +590,7 @@ int ra_ring_bwd(const void* q, const void* k, const void* v, const void* o, ra_d
     a.Dvec = Dv;
     a.B = s.B; a.N = s.Nq; a.Hq = s.Hq; a.Hkv = s.Hkv; a.d = s.d;
     a.q_bs = s.q_bs; a.kv_bs = s.kv_bs;
-    a.scale = scale; a.causal = causal != 0;
+    a.scale = scale; a.causal = causal;
     a.P = P; a.S = s.Nq / P;
     a.dq = dq; a.dk = dk; a.dv = dv; a.grad_dtype = grad_dtype;
     {
@@ -623,8 +629,8 @@ int ra_ring_bwd(const void* q, const void* k, const void* v, const void* o, ra_d
   a.B = s.B; a.N = s.Nq; a.Hq = s.Hq; a.Hkv = s.Hkv; a.d = s.d;
   a.scale = scale;
   a.scale_log2 = scale * 1.4426950408889634f;
-  a.causal = causal != 0;
-  a.ring_P = P; a.ring_S = s.Nq / P;
+  a.causal = causal;
+  a.ring_P = P; a.ring_S = s.Nq / P; a.precise = precise;
   a.lse = lse2; a.Dvec = Dv; a.dq_acc = dq_acc;
   a.dk = dk; a.dv = dv; a.grad_dtype = grad_dtype; a.kv_bs = s.kv_bs;
   a.status = st;

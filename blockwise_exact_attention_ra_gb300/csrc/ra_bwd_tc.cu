@@ -31,6 +31,10 @@
 // dK [256,256+D), dV [256+D,256+2D).
 // MMA order per iteration: dV(i) S(i+1) dK(i) dQ(i) dP(i+1); the compute
 // warps start on S(i+1) while dK(i) and dQ(i) run.
+// With PRECISE, dS enters the dK product as two fp16 terms (hi from shared
+// memory, lo = fp16(dS - hi) from TMEM columns of dP^T that have already been
+// read: [128+64h, 128+64h+32) for query half h), so its rounding drops from
+// 2^-12 relative to about 2^-24; dQ keeps the single fp16 term.
 #include <math.h>
 
 #include "ra_device.cuh"
@@ -114,7 +118,7 @@ __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t n) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
 }
 
-template <int D>
+template <int D, bool PRECISE>
 __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_constant__ TcBwdArgs a) {
   using L = BwdSmem<D>;
   extern __shared__ __align__(1024) uint8_t smem[];
@@ -277,6 +281,13 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
             mma_ss(T_DK, smem_desc_sw128(sDS + off, 16, 1024), smem_desc_sw128(sQ + kk * 2048, 16384, 1024), id_acc,
                    (it > 0 || kk > 0) ? 1u : 0u);
           }
+          if (PRECISE) {  // + dS_lo^T Q_i, dS_lo^T in TMEM (queries 0-63 at dP columns 0-31, 64-127 at 64-95)
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk) {
+              const uint32_t la = T_DP + (kk < 4 ? kk * 8 : 64 + (kk - 4) * 8);
+              mma_ts(T_DK, la, smem_desc_sw128(sQ + kk * 2048, 16384, 1024), id_acc, 1u);
+            }
+          }
           // dQ_i = dS K   (the same dS^T tile read MN-major: M = queries)
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk) {
@@ -356,12 +367,20 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
           RA_TMEM_LD32(tDP + c, dp);
           tmem_ld_wait();
           uint32_t pk[16];
+          uint32_t pl[PRECISE ? 16 : 1];
 #pragma unroll
           for (int j = 0; j < 32; j += 2) {
             const float d0 = __uint_as_float(pr[c + j]) * (__uint_as_float(dp[j]) - dvec[c + j]);
             const float d1 = __uint_as_float(pr[c + j + 1]) * (__uint_as_float(dp[j + 1]) - dvec[c + j + 1]);
             pk[j / 2] = pack_half2(d0, d1);
+            if (PRECISE) {
+              const float2 hi = unpack_half2(pk[j / 2]);
+              pl[j / 2] = pack_half2(d0 - hi.x, d1 - hi.y);
+            }
           }
+          // dP^T columns [c, c+32) of this half have been read: the lo terms go
+          // to its columns [c/2, c/2+16)
+          if (PRECISE) RA_TMEM_ST16(tDP + c / 2, pl);
           // 16-byte chunks (c/8 .. c/8+3) of this row, 128-byte swizzle
 #pragma unroll
           for (int q4 = 0; q4 < 4; ++q4) {
@@ -466,19 +485,21 @@ cudaError_t launch_tc_bwd(TcBwdArgs& a, int num_sms, cudaStream_t st) {
   if (a.num_units <= 0) return cudaSuccess;
   const int grid = a.num_units < num_sms ? a.num_units : num_sms;
   cudaError_t e;
-  if (a.d == 128) {
-    e = cudaFuncSetAttribute(tc_bwd_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             BwdSmem<128>::kBytes);
-    if (e != cudaSuccess) return e;
-    tc_bwd_kernel<128><<<grid, kThreads, BwdSmem<128>::kBytes, st>>>(a);
-  } else if (a.d == 64) {
-    e = cudaFuncSetAttribute(tc_bwd_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             BwdSmem<64>::kBytes);
-    if (e != cudaSuccess) return e;
-    tc_bwd_kernel<64><<<grid, kThreads, BwdSmem<64>::kBytes, st>>>(a);
-  } else {
+  auto run = [&](auto kernel, int smem) {
+    cudaError_t err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (err != cudaSuccess) return err;
+    kernel<<<grid, kThreads, smem, st>>>(a);
+    return cudaSuccess;
+  };
+  if (a.d == 128)
+    e = a.precise ? run(tc_bwd_kernel<128, true>, BwdSmem<128>::kBytes)
+                  : run(tc_bwd_kernel<128, false>, BwdSmem<128>::kBytes);
+  else if (a.d == 64)
+    e = a.precise ? run(tc_bwd_kernel<64, true>, BwdSmem<64>::kBytes)
+                  : run(tc_bwd_kernel<64, false>, BwdSmem<64>::kBytes);
+  else
     return cudaErrorInvalidValue;
-  }
+  if (e != cudaSuccess) return e;
   count_launch();
   return cudaGetLastError();
 }

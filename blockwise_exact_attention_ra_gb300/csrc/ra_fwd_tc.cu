@@ -31,7 +31,10 @@
 //
 // Numerics: S = Q K^T accumulates in fp32 from bf16/fp16 operands; scores
 // are scaled in the exponent (exp2 with log2(e) folded into the scale);
-// P is rounded to fp16 and V is fp16, O accumulates in fp32.  The running
+// P is rounded to fp16 and V is fp16, O accumulates in fp32.  With PRECISE,
+// P is carried as two fp16 terms (hi = fp16(p), lo = fp16(p - hi), the lo
+// term in S_X columns [64,128)) and both are multiplied by V, which brings
+// the rounding of P from 2^-12 relative to about 2^-24.  The running
 // maximum is updated lazily: O and l are rescaled only when the maximum
 // grows by more than 8 (log2 units), so P <= 2^8, well inside fp16.
 #include <math.h>
@@ -153,7 +156,7 @@ __device__ __forceinline__ UnitInfo unit_info(const TcFwdArgs& a, int u) {
   return r;
 }
 
-template <int D>
+template <int D, bool PRECISE>
 __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_constant__ TcFwdArgs a) {
   using L = FwdSmem<D>;
   extern __shared__ uint8_t smem_raw[];
@@ -290,6 +293,11 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
           mma_ts(tO[x], tS[x] + kk * 8, smem_desc_sw128(vb + kk * 2048, 16384, 1024), idesc_pv,
                  (accumulate || kk > 0) ? 1u : 0u);
         }
+        if (PRECISE) {  // + P_lo V
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)
+            mma_ts(tO[x], tS[x] + 64 + kk * 8, smem_desc_sw128(vb + kk * 2048, 16384, 1024), idesc_pv, 1u);
+        }
       };
       for (int u = blockIdx.x; u < a.num_units && ok; u += gridDim.x) {
         const UnitInfo ui = unit_info(a, u);
@@ -415,14 +423,20 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
 #pragma unroll
         for (int c = 0; c < 128; c += 32) {
           uint32_t pk[16];
+          uint32_t pl[PRECISE ? 16 : 1];
 #pragma unroll
           for (int j = 0; j < 32; j += 2) {
             const float p0 = ex2_approx(fmaf(__uint_as_float(sr[c + j]), sl2, neg_m));
             const float p1 = ex2_approx(fmaf(__uint_as_float(sr[c + j + 1]), sl2, neg_m));
             rs += p0 + p1;
             pk[j / 2] = pack_half2(p0, p1);
+            if (PRECISE) {
+              const float2 hi = unpack_half2(pk[j / 2]);
+              pl[j / 2] = pack_half2(p0 - hi.x, p1 - hi.y);
+            }
           }
           RA_TMEM_ST16(tS + c / 2, pk);
+          if (PRECISE) RA_TMEM_ST16(tS + 64 + c / 2, pl);
         }
         l_run = l_run * alpha + rs;
         m_run = m_use;
@@ -517,19 +531,21 @@ cudaError_t launch_tc_fwd(TcFwdArgs& a, int num_sms, cudaStream_t st) {
   if (a.num_units <= 0) return cudaSuccess;
   const int grid = a.num_units < num_sms ? a.num_units : num_sms;
   cudaError_t e;
-  if (a.d == 128) {
-    e = cudaFuncSetAttribute(tc_fwd_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             FwdSmem<128>::kAlloc);
-    if (e != cudaSuccess) return e;
-    tc_fwd_kernel<128><<<grid, kThreads, FwdSmem<128>::kAlloc, st>>>(a);
-  } else if (a.d == 64) {
-    e = cudaFuncSetAttribute(tc_fwd_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             FwdSmem<64>::kAlloc);
-    if (e != cudaSuccess) return e;
-    tc_fwd_kernel<64><<<grid, kThreads, FwdSmem<64>::kAlloc, st>>>(a);
-  } else {
+  auto run = [&](auto kernel, int smem) {
+    cudaError_t err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (err != cudaSuccess) return err;
+    kernel<<<grid, kThreads, smem, st>>>(a);
+    return cudaSuccess;
+  };
+  if (a.d == 128)
+    e = a.precise ? run(tc_fwd_kernel<128, true>, FwdSmem<128>::kAlloc)
+                  : run(tc_fwd_kernel<128, false>, FwdSmem<128>::kAlloc);
+  else if (a.d == 64)
+    e = a.precise ? run(tc_fwd_kernel<64, true>, FwdSmem<64>::kAlloc)
+                  : run(tc_fwd_kernel<64, false>, FwdSmem<64>::kAlloc);
+  else
     return cudaErrorInvalidValue;
-  }
+  if (e != cudaSuccess) return e;
   count_launch();
   return cudaGetLastError();
 }

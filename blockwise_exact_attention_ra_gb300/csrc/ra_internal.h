@@ -96,6 +96,7 @@ struct TcFwdArgs {
   // rows, 128-byte swizzle.  q/k in qk_dtype, v in fp16.
   CUtensorMap tm_q, tm_k, tm_v;
   int qk_bf16;  // 1: q, k are bf16; 0: fp16
+  int precise;  // two-term fp16 P in the P V product
   int B, Nq, Nkv, Hq, Hkv, d;
   float scale_log2;  // scale * log2(e)
   int causal;
@@ -123,6 +124,7 @@ struct TcBwdArgs {
   float scale;
   float scale_log2;
   int causal;
+  int precise;  // two-term fp16 dS in the dK product
   int ring_P, ring_S;
   const float* lse;   // [B, Hq, N], multiplied by log2(e)
   const float* Dvec;  // [B, Hq, N]

@@ -20,8 +20,9 @@
  *   offsets.  The fp32 running state is o_acc [B, N_q, Hq, d] (packed) and
  *   m_acc, l_acc, lse [B, Hq, N_q] (packed).
  * Scores.  s_ij = scale * q_i . k_j; scale is usually d^-0.5 (same section).
- *   With causal != 0 key j is visible to query i iff kv_pos(j) <= q_pos(i),
- *   positions being global row indices (q_off / kv_off added for blocks).
+ *   With RA_CAUSAL in `flags` key j is visible to query i iff
+ *   kv_pos(j) <= q_pos(i), positions being global row indices (q_off /
+ *   kv_off added for blocks).
  * State.  (m, l, o) is the triple the pages carry between ring steps
  *   (max_score, exp_sum, weighted_output; "Gotchas and Failure Modes"):
  *   l = sum_j exp(s_j - m), o = sum_j exp(s_j - m) v_j, m in natural-log
@@ -49,10 +50,10 @@
  *   product, and bf16 operands of those products are copied to fp16 in the
  *   workspace first (exact for |x| in [2^-14, 65504]; larger values set
  *   RA_ERR_RANGE in the status word).
- * Requirements.  Pointers 16-byte aligned; N_q, N_kv, the host block size
- *   and offsets used with tensor cores multiples of 128 rows for
- *   ra_ring_fwd / ra_ring_bwd; violations return RA_ERR_INVALID_ARG or
- *   RA_ERR_UNSUPPORTED.  Nothing falls back to another implementation.
+ * Requirements.  Pointers 16-byte aligned; for ra_ring_fwd / ra_ring_bwd on
+ *   tensor cores the host block N/P is a multiple of 128 rows; violations
+ *   return RA_ERR_INVALID_ARG or RA_ERR_UNSUPPORTED.  Nothing falls back to
+ *   another implementation.
  */
 #ifndef RA_H_
 #define RA_H_
@@ -64,6 +65,16 @@ extern "C" {
 #endif
 
 typedef enum { RA_F32 = 0, RA_BF16 = 1, RA_F16 = 2 } ra_dtype;
+
+/* Bits of the `flags` argument.
+ * RA_CAUSAL   key j is visible to query i only if kv_pos(j) <= q_pos(i).
+ * RA_PRECISE  16-bit inputs: the operand rounded to fp16 for the second
+ *             product (P in P V; dS in dS^T Q) is carried as two fp16 terms
+ *             hi + lo, taking its rounding from 2^-12 to about 2^-24
+ *             relative at the cost of one more MMA per tile.  Needed when
+ *             logits are large and values have outliers (e.g. |q| ~ 4 N(0,1)
+ *             with +-50 entries in V); ignored for RA_F32. */
+enum { RA_CAUSAL = 1, RA_PRECISE = 2 };
 
 typedef enum {
   RA_OK = 0,
@@ -100,15 +111,15 @@ int ra_acc_init(float* o_acc, float* m_acc, float* l_acc, ra_shape shape,
  *   k_blk, v_blk [B, N_kv, Hkv, d]  key/value block at positions kv_off + c
  *   dtype  type of q, k_blk, v_blk
  *   o_acc, m_acc, l_acc  state of the query block, read and updated
- *   causal, scale  as in the conventions above; key/value tiles wholly after
- *          a query tile are skipped, rows left with no visible key keep
- *          their state unchanged
+ *   flags  RA_CAUSAL / RA_PRECISE; key/value tiles wholly after a query
+ *          tile are skipped, rows left with no visible key keep their state
+ *   scale  score scale (> 0)
  *   workspace, ws_bytes  at least ra_block_fwd_workspace_bytes(dtype, shape)
- * Tensor-core dtypes need N_q, N_kv multiples of 128 and d in {64, 128};
- * RA_F32 accepts any N_q, N_kv >= 1 and d in {32, 64, 128}. */
+ * Any N_q, N_kv >= 1 (ragged tiles are masked); tensor-core dtypes need
+ * d in {64, 128}, RA_F32 d in {32, 64, 128}. */
 int ra_block_fwd(const void* q, const void* k_blk, const void* v_blk,
                  ra_dtype dtype, float* o_acc, float* m_acc, float* l_acc,
-                 ra_shape shape, long long q_off, long long kv_off, int causal,
+                 ra_shape shape, long long q_off, long long kv_off, int flags,
                  float scale, void* workspace, size_t ws_bytes, void* stream);
 size_t ra_block_fwd_workspace_bytes(ra_dtype dtype, ra_shape shape);
 
@@ -136,7 +147,7 @@ int ra_finalize(const float* o_acc, const float* m_acc, const float* l_acc,
  *   o [B, N, Hq, d] in o_dtype; lse [B, Hq, N] fp32 (natural log)
  * Tensor-core dtypes need S a multiple of 128. */
 int ra_ring_fwd(const void* q, const void* k, const void* v, ra_dtype dtype,
-                ra_shape shape, int P, int causal, float scale, void* o,
+                ra_shape shape, int P, int flags, float scale, void* o,
                 ra_dtype o_dtype, float* lse, void* workspace, size_t ws_bytes,
                 void* stream);
 size_t ra_ring_fwd_workspace_bytes(ra_dtype dtype, ra_shape shape, int P);
@@ -154,7 +165,7 @@ size_t ra_ring_fwd_workspace_bytes(ra_dtype dtype, ra_shape shape, int P);
  *   dk, dv [B,N,Hkv,d] written in grad_dtype (fully overwritten). */
 int ra_ring_bwd(const void* q, const void* k, const void* v, const void* o,
                 ra_dtype o_dtype, const void* dO, const float* lse,
-                ra_dtype dtype, ra_shape shape, int P, int causal, float scale,
+                ra_dtype dtype, ra_shape shape, int P, int flags, float scale,
                 void* dq, void* dk, void* dv, ra_dtype grad_dtype,
                 void* workspace, size_t ws_bytes, void* stream);
 size_t ra_ring_bwd_workspace_bytes(ra_dtype dtype, ra_dtype grad_dtype,
