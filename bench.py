@@ -374,7 +374,15 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-rows", type=int, default=3072)
     ap.add_argument("--ref-rows", type=int, default=48)
+    ap.add_argument("--N", type=int, default=None, help="override N (profiling on a smaller case)")
+    ap.add_argument("--heads", type=int, default=None, help="override the head count (profiling)")
     args = ap.parse_args()
+    if args.N or args.heads:
+        WORKLOAD["N"] = args.N or WORKLOAD["N"]
+        WORKLOAD["Hq"] = WORKLOAD["Hkv"] = args.heads or WORKLOAD["Hq"]
+        global WORKLOAD_NAME
+        WORKLOAD_NAME = (f"bf16 causal ring attention fwd+bwd, B1 H{WORKLOAD['Hq']} N{WORKLOAD['N']} "
+                         f"d128, P32 (profiling case)")
     if args.warmup < 3:
         args.warmup = 3
     ws, rank, local = dist_env()

@@ -70,14 +70,18 @@ struct BwdUnit {
   int n_iter; // count * group
 };
 
+// Units are ordered head-major: every resident CTA works on the same
+// (batch, key/value head) at a time, so the query tiles, dO tiles and dQ
+// accumulator rows they sweep stay in L2 (one head of them is ~128 MB at
+// N = 131072).  Within a head the earliest key tiles come first: under a
+// causal mask they have the most work.
 __device__ __forceinline__ BwdUnit bwd_unit(const TcBwdArgs& a, int u) {
   BwdUnit r;
-  const int BG = a.B * a.Hkv;
-  const int bg = u % BG;
-  r.jt = u / BG;  // ascending: under a causal mask the earliest keys have the most work
+  const int nT = a.N / 128;
+  const int bg = u / nT;
+  r.jt = u % nT;
   r.b = bg / a.Hkv;
   r.g = bg % a.Hkv;
-  const int nT = a.N / 128;
   r.count = a.causal ? nT - r.jt : nT;
   r.n_iter = r.count * (a.Hq / a.Hkv);
   return r;
@@ -179,8 +183,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
-      const uint64_t pol_kv = policy_evict_first();
-      const uint64_t pol_q = policy_evict_last();
+      const uint64_t pol_kv = policy_evict_first();  // one unit reads its K, V tile once
+      const uint64_t pol_q = policy_evict_normal();  // shared with the CTAs on nearby key tiles
       uint32_t qd_cnt = 0;
       int k = 0;
       bool ok = true;
@@ -344,10 +348,15 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
         const bool diag = a.causal && qt == bu.jt;
         // P^T = exp2(S^T * scale*log2e - LSE*log2e); query column c visible iff c >= key row
 #pragma unroll
-        for (int c = 0; c < 64; ++c) {
-          float p = ex2_approx(fmaf(__uint_as_float(pr[c]), sl2, -lse2[c]));
-          if (diag && half * 64 + c < r) p = 0.f;
-          pr[c] = __float_as_uint(p);
+        for (int c = 0; c < 64; c += 4) {
+          const float4 l4 = *reinterpret_cast<const float4*>(lse2 + c);
+          const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
+#pragma unroll
+          for (int u4 = 0; u4 < 4; ++u4) {
+            float p = ex2_approx(fmaf(__uint_as_float(pr[c + u4]), sl2, -lv[u4]));
+            if (diag && half * 64 + c + u4 < r) p = 0.f;
+            pr[c + u4] = __float_as_uint(p);
+          }
         }
         // P^T (fp16) back into TMEM for the dV MMA
 #pragma unroll
@@ -370,8 +379,9 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
           uint32_t pl[PRECISE ? 16 : 1];
 #pragma unroll
           for (int j = 0; j < 32; j += 2) {
-            const float d0 = __uint_as_float(pr[c + j]) * (__uint_as_float(dp[j]) - dvec[c + j]);
-            const float d1 = __uint_as_float(pr[c + j + 1]) * (__uint_as_float(dp[j + 1]) - dvec[c + j + 1]);
+            const float2 dd = *reinterpret_cast<const float2*>(dvec + c + j);
+            const float d0 = __uint_as_float(pr[c + j]) * (__uint_as_float(dp[j]) - dd.x);
+            const float d1 = __uint_as_float(pr[c + j + 1]) * (__uint_as_float(dp[j + 1]) - dd.y);
             pk[j / 2] = pack_half2(d0, d1);
             if (PRECISE) {
               const float2 hi = unpack_half2(pk[j / 2]);
@@ -412,21 +422,17 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
         ++dq_cnt;
         tc_fence_after();
         float* dst = a.dq_acc + (((long long)bu.b * a.N + (long long)qt * 128 + r) * a.Hq + h) * D;
+        // read the whole dQ row, hand the TMEM columns back, then reduce
+        uint32_t v[D];
 #pragma unroll
-        for (int c = 0; c < D; c += 64) {
-          uint32_t v[64];
-          RA_TMEM_LD32(T_DP + lane_off + c, v);
-          RA_TMEM_LD32(T_DP + lane_off + c + 32, (v + 32));
-          tmem_ld_wait();
-          if (c + 64 >= D) {
-            tc_fence_before();
-            mbar_arrive(BAR_DQ_FREE);
-          }
+        for (int c = 0; c < D; c += 32) RA_TMEM_LD32(T_DP + lane_off + c, (v + c));
+        tmem_ld_wait();
+        tc_fence_before();
+        mbar_arrive(BAR_DQ_FREE);
 #pragma unroll
-          for (int j = 0; j < 64; j += 4)
-            red_add_v4(dst + c + j, __uint_as_float(v[j]), __uint_as_float(v[j + 1]), __uint_as_float(v[j + 2]),
-                       __uint_as_float(v[j + 3]));
-        }
+        for (int j = 0; j < D; j += 4)
+          red_add_v4(dst + j, __uint_as_float(v[j]), __uint_as_float(v[j + 1]), __uint_as_float(v[j + 2]),
+                     __uint_as_float(v[j + 3]));
       }
       if (!ok) break;
       if (!mbar_wait(BAR_DKV_FULL, k & 1, abort_flag, a.status, lim)) { ok = false; break; }

@@ -98,11 +98,21 @@ __device__ __forceinline__ int last_visible_tile(const TcFwdArgs& a, long long q
   return (int)(t < nkt - 1 ? t : nkt - 1);
 }
 
+// Units are ordered head-major (all resident CTAs sweep the key/value tiles
+// of one (batch, head) together, which keeps them in L2), and within a head
+// from the last query tiles to the first: under a causal mask the last ones
+// see the most keys.
 __device__ __forceinline__ UnitInfo unit_info(const TcFwdArgs& a, int u) {
   UnitInfo r;
-  const int BH = a.B * a.Hq;
-  const int bh = u % BH;
-  const int pidx_desc = u / BH;
+  int per_head;
+  if (a.ring_P > 0) {
+    const int T = a.ring_S / 128;
+    per_head = a.ring_P * ((T + 1) / 2);
+  } else {
+    per_head = (((a.Nq + 127) / 128) + 1) / 2;
+  }
+  const int bh = u / per_head;
+  const int pidx_desc = u % per_head;
   r.b = bh / a.Hq;
   r.h = bh % a.Hq;
   r.g = r.h / (a.Hq / a.Hkv);
