@@ -32,7 +32,9 @@ STATUS = {0: "RA_OK", 1: "RA_ERR_INVALID_ARG", 2: "RA_ERR_UNSUPPORTED", 3: "RA_E
 _DTYPES = {torch.float32: RA_F32, torch.bfloat16: RA_BF16, torch.float16: RA_F16}
 _TORCH = {v: k for k, v in _DTYPES.items()}
 
-_LIBPATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libra.so")
+# RA_LIBRARY may name another build of the same library (e.g. an instrumented one).
+_LIBPATH = os.environ.get("RA_LIBRARY") or os.path.join(os.path.dirname(os.path.abspath(__file__)),
+                                                        "libra.so")
 
 
 class RAError(RuntimeError):

@@ -146,6 +146,22 @@ int make_map(CUtensorMap* m, const void* base, int is_bf16, int B, int N, int H,
   return RA_OK;
 }
 
+// Packed fp32 [B, N, H, d] tensor: box (32, 1, 128, 1), 128-byte swizzle.
+int make_map_f32(CUtensorMap* m, void* base, int B, int N, int H, int d) {
+  EncodeTiledFn fn;
+  int rc = encoder(&fn);
+  if (rc) return rc;
+  cuuint64_t dims[4] = {(cuuint64_t)d, (cuuint64_t)H, (cuuint64_t)N, (cuuint64_t)B};
+  cuuint64_t strides[3] = {(cuuint64_t)d * 4, (cuuint64_t)H * d * 4, (cuuint64_t)N * H * d * 4};
+  cuuint32_t box[4] = {32, 1, 128, 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, base, dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(RA_ERR_CUDA, "cuTensorMapEncodeTiled (fp32) failed (%d)", (int)r);
+  return RA_OK;
+}
+
 // -------------------------------------------------------------- validation
 size_t dtype_size(int dt) { return dt == RA_F32 ? 4 : 2; }
 bool valid_dtype(int dt) { return dt == RA_F32 || dt == RA_BF16 || dt == RA_F16; }
@@ -624,7 +640,8 @@ int ra_ring_bwd(const void* q, const void* k, const void* v, const void* o, ra_d
   if ((rc = make_map(&a.tm_q, q16, 0, s.B, s.Nq, s.Hq, s.d, q16_bs)) ||
       (rc = make_map(&a.tm_do, do16, 0, s.B, s.Nq, s.Hq, s.d, q16_bs)) ||
       (rc = make_map(&a.tm_k, k16, 0, s.B, s.Nkv, s.Hkv, s.d, kv16_bs)) ||
-      (rc = make_map(&a.tm_v, v16, 0, s.B, s.Nkv, s.Hkv, s.d, kv16_bs)))
+      (rc = make_map(&a.tm_v, v16, 0, s.B, s.Nkv, s.Hkv, s.d, kv16_bs)) ||
+      (rc = make_map_f32(&a.tm_dq, dq_acc, s.B, s.Nq, s.Hq, s.d)))
     return rc;
   a.B = s.B; a.N = s.Nq; a.Hq = s.Hq; a.Hkv = s.Hkv; a.d = s.d;
   a.scale = scale;

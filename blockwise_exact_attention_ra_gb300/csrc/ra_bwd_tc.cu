@@ -23,9 +23,16 @@
 //   warp 1       TMEM allocation; one lane issues every tcgen05.mma
 //   warps 2-9    compute: thread = key row; warps 2-5 take query columns
 //                0-63, warps 6-9 columns 64-127
-//   warps 10-13  dQ: read dQ_i from TMEM (thread = query row) and reduce-add
-//                it into the fp32 accumulator; at the end of a unit write
+//   warps 10-13  dQ: read dQ_i from TMEM (thread = query row), stage it in
+//                shared memory and reduce-add it into the fp32 accumulator
+//                with TMA (whole 128-byte lines); at the end of a unit write
 //                dK, dV
+// Shared memory has no room for a dQ buffer, but once dQ_i is complete every
+// MMA that reads Q_i and dO_i has completed too, so the dQ warps stage dQ_i
+// in that stage's Q and dO buffers (together exactly 128 x D fp32) and hand
+// the stage back to the producer once the TMA engine has read it.  (Per-thread
+// red.global of whole rows cost ~6000 cycles per tile in the load/store unit
+// and starved the compute warps' shared-memory traffic.)
 // TMEM (512 columns): S^T [0,128) (P^T as fp16 written back into columns
 // [0,32) and [64,96)), dP^T [128,256) (dQ_i reuses [128,128+D)),
 // dK [256,256+D), dV [256+D,256+2D).
@@ -56,8 +63,8 @@ struct BwdSmem {
   static constexpr int kVec0 = kDS + kDSBytes;  // per stage: LSE*log2e [128], D [128]
   static constexpr int kBars = kVec0 + 2 * 1024;
   // kv_full, kv_empty, qd_full[2], qd_empty[2], s_full, dp_full, ds_full,
-  // ds_free, dq_full, dq_free, dkv_full, dkv_free, drain
-  static constexpr int kNumBars = 15;
+  // ds_free, dq_full, dq_free, dkv_full, dkv_free, drain, dq_staged
+  static constexpr int kNumBars = 16;
   static constexpr int kMisc = kBars + kNumBars * 8;
   static constexpr int kUsed = kMisc + 16;
   // at least 120 KB so that one CTA (holding all 512 TMEM columns) occupies an SM
@@ -112,14 +119,29 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
       : "memory");
 }
 
-__device__ __forceinline__ void red_add_v4(float* p, float a, float b, float c, float d) {
-  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(a), "f"(b), "f"(c),
-               "f"(d)
-               : "memory");
+// TMA reduce-add of one 128-row x 32-column fp32 box from shared memory.
+__device__ __forceinline__ void tma_reduce_add_4d(const CUtensorMap* map, uint32_t src, int c0, int c1,
+                                                  int c2, int c3) {
+  asm volatile(
+      "cp.reduce.async.bulk.tensor.4d.global.shared::cta.add.tile.bulk_group [%0, {%2, %3, %4, %5}], [%1];" ::"l"(
+          map),
+      "r"(src), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+      : "memory");
 }
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read_all() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
-__device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t n) {
-  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+// Shared-memory offset of dQ staging box c (32 fp32 columns x 128 rows, 16 KB)
+// of stage s: the Q buffer holds the first kTile / 16 KB boxes, the dO buffer
+// the rest.
+template <int D>
+__device__ __forceinline__ uint32_t dq_box(int s, int c) {
+  using L = BwdSmem<D>;
+  constexpr int per = L::kTile / 16384;
+  return c < per ? L::kQ0 + s * L::kTile + c * 16384 : L::kDO0 + s * L::kTile + (c - per) * 16384;
 }
 
 template <int D, bool PRECISE>
@@ -137,7 +159,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
   auto bar_qd_empty = [&](int s) { return bar0 + 32 + 8 * s; };
   const uint32_t BAR_S_FULL = bar0 + 48, BAR_DP_FULL = bar0 + 56, BAR_DS_FULL = bar0 + 64,
                  BAR_DS_FREE = bar0 + 72, BAR_DQ_FULL = bar0 + 80, BAR_DQ_FREE = bar0 + 88,
-                 BAR_DKV_FULL = bar0 + 96, BAR_DKV_FREE = bar0 + 104, BAR_DRAIN = bar0 + 112;
+                 BAR_DKV_FULL = bar0 + 96, BAR_DKV_FREE = bar0 + 104, BAR_DRAIN = bar0 + 112,
+                 BAR_DQ_STAGED = bar0 + 120;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kMisc + 4);
   const uint32_t warp = warp_id();
@@ -160,6 +183,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
     mbar_init(BAR_DKV_FULL, 1);
     mbar_init(BAR_DKV_FREE, 128);
     mbar_init(BAR_DRAIN, 1);
+    mbar_init(BAR_DQ_STAGED, 128);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -172,6 +196,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
     tma_prefetch_desc(&a.tm_k);
     tma_prefetch_desc(&a.tm_v);
     tma_prefetch_desc(&a.tm_do);
+    tma_prefetch_desc(&a.tm_dq);
   }
   tc_fence_before();
   __syncthreads();
@@ -298,10 +323,9 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
             mma_ss(T_DP, smem_desc_sw128(sDS + kk * 2048, 16384, 1024), smem_desc_sw128(sK + kk * 2048, 16384, 1024),
                    id_dq, kk > 0 ? 1u : 0u);
           }
-          mma_commit(BAR_DQ_FULL);
+          mma_commit(BAR_DQ_FULL);  // also means Q_i, dO_i are consumed; the dQ warps release the stage
           ++dq_cnt;
           mma_commit(BAR_DS_FREE);
-          mma_commit(bar_qd_empty(s));
           ++qd_cnt;
           if (has_next) {
             if (!wait(BAR_DQ_FREE, (dq_cnt - 1) & 1)) break;
@@ -421,18 +445,40 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
         if (!mbar_wait(BAR_DQ_FULL, dq_cnt & 1, abort_flag, a.status, lim)) { ok = false; break; }
         ++dq_cnt;
         tc_fence_after();
-        float* dst = a.dq_acc + (((long long)bu.b * a.N + (long long)qt * 128 + r) * a.Hq + h) * D;
-        // read the whole dQ row, hand the TMEM columns back, then reduce
-        uint32_t v[D];
+        const int s = (dq_cnt - 1) & 1;  // the stage that held Q_i, dO_i
+        // read the dQ row 64 columns at a time (register budget), hand the
+        // TMEM columns back after the last read, and stage it: box c, row r,
+        // 16-byte chunk j at r * 128 + ((j ^ (r & 7)) << 4) (128-byte swizzle)
 #pragma unroll
-        for (int c = 0; c < D; c += 32) RA_TMEM_LD32(T_DP + lane_off + c, (v + c));
-        tmem_ld_wait();
-        tc_fence_before();
-        mbar_arrive(BAR_DQ_FREE);
+        for (int c0 = 0; c0 < D; c0 += 64) {
+          uint32_t v[64];
+          RA_TMEM_LD32(T_DP + lane_off + c0, v);
+          RA_TMEM_LD32(T_DP + lane_off + c0 + 32, (v + 32));
+          tmem_ld_wait();
+          if (c0 + 64 >= D) {
+            tc_fence_before();
+            mbar_arrive(BAR_DQ_FREE);
+          }
 #pragma unroll
-        for (int j = 0; j < D; j += 4)
-          red_add_v4(dst + j, __uint_as_float(v[j]), __uint_as_float(v[j + 1]), __uint_as_float(v[j + 2]),
-                     __uint_as_float(v[j + 3]));
+          for (int cc = 0; cc < 2; ++cc) {
+            uint8_t* box = smem + dq_box<D>(s, c0 / 32 + cc) + r * 128;
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+              *reinterpret_cast<uint4*>(box + ((j ^ (r & 7)) << 4)) =
+                  make_uint4(v[32 * cc + 4 * j], v[32 * cc + 4 * j + 1], v[32 * cc + 4 * j + 2], v[32 * cc + 4 * j + 3]);
+          }
+        }
+        fence_proxy_async_smem();
+        mbar_arrive(BAR_DQ_STAGED);
+        if (warp == 10 && lane == 0) {
+          if (!mbar_wait(BAR_DQ_STAGED, (dq_cnt - 1) & 1, abort_flag, a.status, lim)) { ok = false; break; }
+#pragma unroll
+          for (int c = 0; c < D / 32; ++c)
+            tma_reduce_add_4d(&a.tm_dq, sbase + dq_box<D>(s, c), 32 * c, h, qt * 128, bu.b);
+          bulk_commit();
+          bulk_wait_read_all();  // the stage may be refilled once the TMA engine has read it
+          mbar_arrive(bar_qd_empty(s));
+        }
       }
       if (!ok) break;
       if (!mbar_wait(BAR_DKV_FULL, k & 1, abort_flag, a.status, lim)) { ok = false; break; }
@@ -477,6 +523,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
       tc_fence_before();
       mbar_arrive(BAR_DKV_FREE);
     }
+    if (warp == 10 && lane == 0) bulk_wait_all();  // reductions complete before the CTA exits
   }
 
   tc_fence_before();

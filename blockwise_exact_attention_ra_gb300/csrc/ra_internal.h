@@ -120,6 +120,9 @@ cudaError_t launch_tc_fwd(TcFwdArgs& a, int num_sms, cudaStream_t st);
 struct TcBwdArgs {
   // fp16 operands: q, dO over [B, N, Hq, d]; k, v over [B, N, Hkv, d]
   CUtensorMap tm_q, tm_k, tm_v, tm_do;
+  // the fp32 dQ accumulator [B, N, Hq, d]: 32-column boxes of 128 rows,
+  // 128-byte swizzle, written by TMA reduce-add
+  CUtensorMap tm_dq;
   int B, N, Hq, Hkv, d;
   float scale;
   float scale_log2;
