@@ -19,6 +19,7 @@ __all__ = [
     "RAError", "RaShape", "lib", "shape_of",
     "ra_acc_init", "ra_block_fwd", "ra_block_fwd_workspace_bytes", "ra_merge", "ra_finalize",
     "ra_ring_fwd", "ra_ring_fwd_workspace_bytes", "ra_ring_bwd", "ra_ring_bwd_workspace_bytes",
+    "ra_ring_fwd_noalloc",
     "ra_sync_status", "ra_last_error", "ra_launch_count", "ra_selftest_timeout",
     "ra_kernel_timing", "ra_kernel_timing_read",
     "ring_attention_fwd", "ring_attention_bwd", "RA_F32", "RA_BF16", "RA_F16",
@@ -65,6 +66,7 @@ def _load():
         "ra_finalize": (i, [vp, vp, vp, vp, i, vp, sh, vp]),
         "ra_ring_fwd": (i, [vp, vp, vp, i, sh, i, i, f, vp, i, vp, vp, sz, vp]),
         "ra_ring_fwd_workspace_bytes": (sz, [i, sh, i]),
+        "ra_ring_fwd_noalloc": (i, [vp, vp, vp, i, sh, i, i, f, vp, i, vp, vp]),
         "ra_ring_bwd": (i, [vp, vp, vp, vp, i, vp, vp, i, sh, i, i, f, vp, vp, vp, i, vp, sz, vp]),
         "ra_ring_bwd_workspace_bytes": (sz, [i, i, sh, i]),
         "ra_sync_status": (i, [vp]),
@@ -200,6 +202,17 @@ def ra_ring_fwd(q, k, v, P, causal, scale, o, lse, workspace=None, stream=None, 
     _check(lib.ra_ring_fwd(_ptr(q), _ptr(k), _ptr(v), _dt(q), shape, int(P), _flags(causal, precise),
                            float(scale), _ptr(o), _dt(o), _ptr(lse), _ptr(workspace), ws_bytes,
                            _stream(stream)))
+
+
+def ra_ring_fwd_noalloc(q, k, v, P, causal, scale, o, lse, stream=None, precise=False):
+    """ra_ring_fwd without a workspace, for callers that cannot allocate device
+    memory: the library's own 32 MiB per-device scratch buffer is used instead
+    (shapes needing more are rejected).  Calls that overlap on the GPU race on
+    that buffer."""
+    shape = shape_of(q, k)
+    _check(lib.ra_ring_fwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _dt(q), shape, int(P),
+                                   _flags(causal, precise), float(scale), _ptr(o), _dt(o),
+                                   _ptr(lse), _stream(stream)))
 
 
 def ra_ring_bwd_workspace_bytes(dtype, grad_dtype, shape, P):

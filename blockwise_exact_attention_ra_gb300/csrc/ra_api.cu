@@ -261,6 +261,12 @@ struct TimedLaunch {
 };
 
 }  // namespace
+
+int set_error(int code, const char* msg) {
+  t_err = msg;
+  return code;
+}
+
 }  // namespace ra
 
 using namespace ra;

@@ -145,4 +145,7 @@ cudaError_t launch_tc_bwd(TcBwdArgs& a, int num_sms, cudaStream_t st);
 // Counts kernel launches (ra_launch_count).
 void count_launch(unsigned n = 1);
 
+// Records `msg` as the calling thread's ra_last_error() message; returns code.
+int set_error(int code, const char* msg);
+
 }  // namespace ra

@@ -1,0 +1,67 @@
+// ra_ring_fwd_noalloc: the ring forward for callers that cannot allocate
+// device memory (see include/ra.h).  The scratch that ra_ring_fwd takes as a
+// caller workspace (the fp16 copy of V for bf16 inputs) lives here in a
+// fixed, file-scope device array instead.
+#include <cuda_runtime.h>
+#include <stdio.h>
+
+#include <mutex>
+
+#include "ra_internal.h"
+
+namespace {
+
+constexpr size_t kScratchBytes = size_t(32) << 20;  // 32 MiB per device
+
+// One copy per device that loads the library; it lives until the process
+// exits.  In host code `g_noalloc_scratch` names a host-side stand-in, not a
+// device address: only the pointer from cudaGetSymbolAddress may be passed
+// to kernels.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kScratchBytes];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+void* g_scratch_ptr[kMaxDevices] = {};
+
+}  // namespace
+
+extern "C" {
+#pragma GCC visibility push(default)
+
+int ra_ring_fwd_noalloc(const void* q, const void* k, const void* v, ra_dtype dtype,
+                        ra_shape shape, int P, int flags, float scale, void* o,
+                        ra_dtype o_dtype, float* lse, void* stream) {
+  const size_t need = ra_ring_fwd_workspace_bytes(dtype, shape, P);
+  if (need > kScratchBytes) {
+    char msg[256];
+    snprintf(msg, sizeof msg,
+             "ra_ring_fwd_noalloc: this shape needs %zu bytes of scratch but the built-in buffer "
+             "holds %zu; call ra_ring_fwd with a workspace instead",
+             need, kScratchBytes);
+    return ra::set_error(RA_ERR_INVALID_ARG, msg);
+  }
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
+    return ra::set_error(RA_ERR_CUDA, "ra_ring_fwd_noalloc: no usable current device");
+  void* scratch = nullptr;
+  {
+    // set-up, once per device, with that device current
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!g_scratch_ptr[dev]) {
+      void* p = nullptr;
+      const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+      if (e != cudaSuccess || !p) {
+        char msg[256];
+        snprintf(msg, sizeof msg, "ra_ring_fwd_noalloc: cudaGetSymbolAddress(scratch) failed: %s",
+                 cudaGetErrorString(e));
+        return ra::set_error(RA_ERR_CUDA, msg);
+      }
+      g_scratch_ptr[dev] = p;
+    }
+    scratch = g_scratch_ptr[dev];
+  }
+  return ra_ring_fwd(q, k, v, dtype, shape, P, flags, scale, o, o_dtype, lse, scratch,
+                     kScratchBytes, stream);
+}
+
+}  // extern "C"

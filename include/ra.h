@@ -171,6 +171,29 @@ int ra_ring_bwd(const void* q, const void* k, const void* v, const void* o,
 size_t ra_ring_bwd_workspace_bytes(ra_dtype dtype, ra_dtype grad_dtype,
                                    ra_shape shape, int P);
 
+/* ra_ring_fwd for callers that cannot allocate device memory: code that runs
+ * where cudaMalloc is not available or not allowed (inside a host callback
+ * or a custom allocator's own hooks, under a framework that owns every
+ * device allocation, or with a fixed memory budget set at start-up) cannot
+ * provide the workspace ra_ring_fwd asks for.  This entry point takes the
+ * same arguments minus the workspace and uses a scratch buffer that is part
+ * of the library itself: a 32 MiB device array per GPU that loads the
+ * library, held until the process exits.  It allocates nothing.  The pages
+ * describe no counterpart; it is a packaging of the same computation.
+ *   Limit: shapes whose ra_ring_fwd_workspace_bytes() exceeds 32 MiB (the
+ *   fp16 copy of V for bf16 inputs, B*N*Hkv*d*2 bytes) are rejected with
+ *   RA_ERR_INVALID_ARG; fp16 and fp32 inputs need no scratch.
+ *   The first call on each device looks up the buffer's device address
+ *   (cudaGetSymbolAddress) with that device current; make that first call
+ *   before any stream capture.
+ *   All calls share the one buffer per device and it keeps whatever the last
+ *   call left there (each call overwrites the part it uses, nothing needs to
+ *   start at zero).  Calls whose work overlaps on the GPU (different streams,
+ *   or threads without ordering between them) race on it. */
+int ra_ring_fwd_noalloc(const void* q, const void* k, const void* v, ra_dtype dtype,
+                        ra_shape shape, int P, int flags, float scale, void* o,
+                        ra_dtype o_dtype, float* lse, void* stream);
+
 /* Synchronise `stream`, then return and clear the device status word
  * (RA_OK, RA_ERR_RANGE or RA_ERR_TIMEOUT), or RA_ERR_CUDA if the stream
  * itself reports an error. */
