@@ -124,6 +124,22 @@ class ClockSampler:
                 "reasons": sorted(reasons)}
 
 
+def max_over_ranks(x, device):
+    """Max of a per-rank float over all ranks (identity on one process)."""
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_value(world_size, flop_per_step_per_rank, ms_per_step):
+    """Whole-job TFLOP/s: every rank runs one replica's step; the step takes
+    the slowest rank's time."""
+    return world_size * flop_per_step_per_rank / (ms_per_step * 1e-3) / 1e12
+
+
 def dist_env():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -268,12 +284,8 @@ def run_ours(args, ws, rank, local):
     ktime = {kid: ra.ra_kernel_timing_read(kid) for kid in (ra.RA_KERNEL_FWD_TC, ra.RA_KERNEL_BWD_TC)}
     ra.ra_kernel_timing(0)
 
-    ms_step = total_ms / args.steps
-    if ws > 1:
-        t = torch.tensor([ms_step], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms_step = float(t.item())
-    value = ws * (fwd_fl + bwd_fl) / (ms_step * 1e-3) / 1e12
+    ms_step = max_over_ranks(total_ms / args.steps, dev)
+    value = job_value(ws, fwd_fl + bwd_fl, ms_step)
     peaks = load_peaks()
 
     # dominant kernel: the one with the larger share of device time
@@ -327,12 +339,8 @@ def run_ours(args, ws, rank, local):
         b.record(stream)
         torch.cuda.synchronize(dev)
         ra.ra_sync_status(stream)
-        e_ms = a.elapsed_time(b) / args.steps
-        if ws > 1:
-            t = torch.tensor([e_ms], device=dev)
-            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-            e_ms = float(t.item())
-        e2e = {"value": ws * (fwd_fl + bwd_fl) / (e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+        e_ms = max_over_ranks(a.elapsed_time(b) / args.steps, dev)
+        e2e = {"value": job_value(ws, fwd_fl + bwd_fl, e_ms), "unit": "TFLOP/s",
                "ms_per_step": e_ms,
                "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in hq),
                "d2h_bytes_per_step": sum(t.numel() * t.element_size() for t in host_out)}
