@@ -27,10 +27,13 @@
 //                shared memory and reduce-add it into the fp32 accumulator
 //                with TMA (whole 128-byte lines); at the end of a unit write
 //                dK, dV
-// Shared memory has no room for a dQ buffer, but once dQ_i is complete every
-// MMA that reads Q_i and dO_i has completed too, so the dQ warps stage dQ_i
-// in that stage's Q and dO buffers (together exactly 128 x D fp32) and hand
-// the stage back to the producer once the TMA engine has read it.  (Per-thread
+// Shared memory has no room for a dQ buffer, but once dQ_i is complete the
+// last MMA that reads dO_i (dV) has completed too, so the dQ warps stage dQ_i
+// in that stage's dO buffer, in two rounds of D/2 columns, and hand the dO
+// buffer back to the producer once the TMA engine has read the second round.
+// Q and dO have separate stage barriers: the Q buffer returns to the producer
+// as soon as dK has consumed it, so the next query tile's S MMA never waits
+// for a reduction (dO_{i+2} is needed latest in an iteration).  (Per-thread
 // red.global of whole rows cost ~6000 cycles per tile in the load/store unit
 // and starved the compute warps' shared-memory traffic.)
 // TMEM (512 columns): S^T [0,128) (P^T as fp16 written back into columns
@@ -62,9 +65,10 @@ struct BwdSmem {
   static constexpr int kDSBytes = 128 * 128 * 2;
   static constexpr int kVec0 = kDS + kDSBytes;  // per stage: LSE*log2e [128], D [128]
   static constexpr int kBars = kVec0 + 2 * 1024;
-  // kv_full, kv_empty, qd_full[2], qd_empty[2], s_full, dp_full, ds_full,
-  // ds_free, dq_full, dq_free, dkv_full, dkv_free, drain, dq_staged
-  static constexpr int kNumBars = 16;
+  // kv_full, kv_empty, q_full[2], q_empty[2], s_full, dp_full, ds_full,
+  // ds_free, dq_full, dq_free, dkv_full, dkv_free, drain, dq_staged,
+  // do_full[2], do_empty[2], dq_drained
+  static constexpr int kNumBars = 21;
   static constexpr int kMisc = kBars + kNumBars * 8;
   static constexpr int kUsed = kMisc + 16;
   // at least 120 KB so that one CTA (holding all 512 TMEM columns) occupies an SM
@@ -134,14 +138,12 @@ __device__ __forceinline__ void bulk_wait_read_all() {
 }
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
-// Shared-memory offset of dQ staging box c (32 fp32 columns x 128 rows, 16 KB)
-// of stage s: the Q buffer holds the first kTile / 16 KB boxes, the dO buffer
-// the rest.
+// dQ staging: round r (columns [r*D/2, (r+1)*D/2)) of stage s goes to the
+// dO buffer of that stage as D/64 boxes of 32 fp32 columns x 128 rows (16 KB).
 template <int D>
-__device__ __forceinline__ uint32_t dq_box(int s, int c) {
+__device__ __forceinline__ uint32_t dq_box(int s, int cc) {
   using L = BwdSmem<D>;
-  constexpr int per = L::kTile / 16384;
-  return c < per ? L::kQ0 + s * L::kTile + c * 16384 : L::kDO0 + s * L::kTile + (c - per) * 16384;
+  return L::kDO0 + s * L::kTile + cc * 16384;
 }
 
 template <int D, bool PRECISE>
@@ -155,8 +157,11 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
   }
   const uint32_t bar0 = sbase + L::kBars;
   const uint32_t BAR_KV_FULL = bar0, BAR_KV_EMPTY = bar0 + 8;
-  auto bar_qd_full = [&](int s) { return bar0 + 16 + 8 * s; };
-  auto bar_qd_empty = [&](int s) { return bar0 + 32 + 8 * s; };
+  auto bar_q_full = [&](int s) { return bar0 + 16 + 8 * s; };
+  auto bar_q_empty = [&](int s) { return bar0 + 32 + 8 * s; };
+  auto bar_do_full = [&](int s) { return bar0 + 128 + 8 * s; };
+  auto bar_do_empty = [&](int s) { return bar0 + 144 + 8 * s; };
+  const uint32_t BAR_DQ_DRAINED = bar0 + 160;
   const uint32_t BAR_S_FULL = bar0 + 48, BAR_DP_FULL = bar0 + 56, BAR_DS_FULL = bar0 + 64,
                  BAR_DS_FREE = bar0 + 72, BAR_DQ_FULL = bar0 + 80, BAR_DQ_FREE = bar0 + 88,
                  BAR_DKV_FULL = bar0 + 96, BAR_DKV_FREE = bar0 + 104, BAR_DRAIN = bar0 + 112,
@@ -171,8 +176,10 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
     mbar_init(BAR_KV_FULL, 1);
     mbar_init(BAR_KV_EMPTY, 1);
     for (int s = 0; s < 2; ++s) {
-      mbar_init(bar_qd_full(s), 1);
-      mbar_init(bar_qd_empty(s), 1);
+      mbar_init(bar_q_full(s), 1);
+      mbar_init(bar_q_empty(s), 1);
+      mbar_init(bar_do_full(s), 1);
+      mbar_init(bar_do_empty(s), 1);
     }
     mbar_init(BAR_S_FULL, 1);
     mbar_init(BAR_DP_FULL, 1);
@@ -184,6 +191,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
     mbar_init(BAR_DKV_FREE, 128);
     mbar_init(BAR_DRAIN, 1);
     mbar_init(BAR_DQ_STAGED, 128);
+    mbar_init(BAR_DQ_DRAINED, 1);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -211,6 +219,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
       const uint64_t pol_kv = policy_evict_first();  // one unit reads its K, V tile once
       const uint64_t pol_q = policy_evict_normal();  // shared with the CTAs on nearby key tiles
       uint32_t qd_cnt = 0;
+      int q_issued[2] = {0, 0}, do_issued[2] = {0, 0};
       int k = 0;
       bool ok = true;
       for (int u = blockIdx.x; u < a.num_units && ok; u += gridDim.x, ++k) {
@@ -226,27 +235,34 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
           int h, qt;
           bwd_iter(a, bu, it, &h, &qt);
           const int s = qd_cnt & 1;
-          if (!mbar_wait(bar_qd_empty(s), ((qd_cnt >> 1) & 1) ^ 1, abort_flag, a.status, lim)) { ok = false; break; }
-          mbar_arrive_expect_tx(bar_qd_full(s), 2 * L::kTile + 1024);
+          const uint32_t par = ((qd_cnt >> 1) & 1) ^ 1;
+          if (!mbar_wait(bar_q_empty(s), par, abort_flag, a.status, lim)) { ok = false; break; }
+          mbar_arrive_expect_tx(bar_q_full(s), L::kTile + 1024);
 #pragma unroll
-          for (int c = 0; c < D / 64; ++c) {
-            tma_load_4d(sbase + L::kQ0 + s * L::kTile + c * 16384, &a.tm_q, bar_qd_full(s), c * 64, h, qt * 128, bu.b, pol_q);
-            tma_load_4d(sbase + L::kDO0 + s * L::kTile + c * 16384, &a.tm_do, bar_qd_full(s), c * 64, h, qt * 128, bu.b, pol_q);
-          }
+          for (int c = 0; c < D / 64; ++c)
+            tma_load_4d(sbase + L::kQ0 + s * L::kTile + c * 16384, &a.tm_q, bar_q_full(s), c * 64, h, qt * 128, bu.b, pol_q);
           const long long vrow = ((long long)bu.b * a.Hq + h) * a.N + (long long)qt * 128;
-          bulk_load(sbase + L::kVec0 + s * 1024, a.lse + vrow, 512, bar_qd_full(s));
-          bulk_load(sbase + L::kVec0 + s * 1024 + 512, a.Dvec + vrow, 512, bar_qd_full(s));
+          bulk_load(sbase + L::kVec0 + s * 1024, a.lse + vrow, 512, bar_q_full(s));
+          bulk_load(sbase + L::kVec0 + s * 1024 + 512, a.Dvec + vrow, 512, bar_q_full(s));
+          q_issued[s] = 1;
+          if (!mbar_wait(bar_do_empty(s), par, abort_flag, a.status, lim)) { ok = false; break; }
+          mbar_arrive_expect_tx(bar_do_full(s), L::kTile);
+#pragma unroll
+          for (int c = 0; c < D / 64; ++c)
+            tma_load_4d(sbase + L::kDO0 + s * L::kTile + c * 16384, &a.tm_do, bar_do_full(s), c * 64, h, qt * 128, bu.b, pol_q);
+          do_issued[s] = 1;
           ++qd_cnt;
         }
       }
       if (*abort_flag) {
         const uint64_t drain = 100000000ull;
         (void)mbar_wait(BAR_KV_FULL, (k - 1) & 1, abort_flag, nullptr, drain);
-        for (int s = 0; s < 2; ++s)
-          if (qd_cnt > (uint32_t)s) {
-            const uint32_t last = ((qd_cnt - 1 - s) & ~1u) + s;  // last load issued on stage s
-            (void)mbar_wait(bar_qd_full(s), (last >> 1) & 1, abort_flag, nullptr, drain);
-          }
+        for (int s = 0; s < 2; ++s) {
+          // phase of the last load issued on stage s (loads alternate stages)
+          const uint32_t last = qd_cnt > (uint32_t)s ? ((qd_cnt - 1 - s) & ~1u) + s : 0;
+          if (q_issued[s]) (void)mbar_wait(bar_q_full(s), (last >> 1) & 1, abort_flag, nullptr, drain);
+          if (do_issued[s]) (void)mbar_wait(bar_do_full(s), (last >> 1) & 1, abort_flag, nullptr, drain);
+        }
       }
     }
   } else if (warp == 1) {
@@ -279,10 +295,11 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
         if (!wait(BAR_KV_FULL, k & 1)) break;
         // prologue: S(0), dP(0)
         uint32_t s = qd_cnt & 1;
-        if (!wait(bar_qd_full(s), (qd_cnt >> 1) & 1)) break;
+        if (!wait(bar_q_full(s), (qd_cnt >> 1) & 1)) break;
         mma_nt(T_S, sK, sbase + L::kQ0 + s * L::kTile);
         mma_commit(BAR_S_FULL);
         if (dq_cnt > 0 && !wait(BAR_DQ_FREE, (dq_cnt - 1) & 1)) break;
+        if (!wait(bar_do_full(s), (qd_cnt >> 1) & 1)) break;
         mma_nt(T_DP, sV, sbase + L::kDO0 + s * L::kTile);
         mma_commit(BAR_DP_FULL);
         for (int it = 0; it < bu.n_iter; ++it) {
@@ -297,9 +314,9 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
             mma_ts(T_DV, pa, smem_desc_sw128(sDO + kk * 2048, 16384, 1024), id_acc, (it > 0 || kk > 0) ? 1u : 0u);
           }
           const bool has_next = it + 1 < bu.n_iter;
-          const uint32_t s2 = (qd_cnt + 1) & 1;
+          const uint32_t s2 = (qd_cnt + 1) & 1, par2 = ((qd_cnt + 1) >> 1) & 1;
           if (has_next) {
-            if (!wait(bar_qd_full(s2), ((qd_cnt + 1) >> 1) & 1)) break;
+            if (!wait(bar_q_full(s2), par2)) break;
             mma_nt(T_S, sK, sbase + L::kQ0 + s2 * L::kTile);
             mma_commit(BAR_S_FULL);
           }
@@ -317,18 +334,20 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
               mma_ts(T_DK, la, smem_desc_sw128(sQ + kk * 2048, 16384, 1024), id_acc, 1u);
             }
           }
+          mma_commit(bar_q_empty(s));  // dK was the last reader of Q_i
           // dQ_i = dS K   (the same dS^T tile read MN-major: M = queries)
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk) {
             mma_ss(T_DP, smem_desc_sw128(sDS + kk * 2048, 16384, 1024), smem_desc_sw128(sK + kk * 2048, 16384, 1024),
                    id_dq, kk > 0 ? 1u : 0u);
           }
-          mma_commit(BAR_DQ_FULL);  // also means Q_i, dO_i are consumed; the dQ warps release the stage
+          mma_commit(BAR_DQ_FULL);  // dO_i is consumed too; the dQ warps stage dQ_i in its buffer
           ++dq_cnt;
           mma_commit(BAR_DS_FREE);
           ++qd_cnt;
           if (has_next) {
             if (!wait(BAR_DQ_FREE, (dq_cnt - 1) & 1)) break;
+            if (!wait(bar_do_full(s2), par2)) break;
             mma_nt(T_DP, sV, sbase + L::kDO0 + s2 * L::kTile);
             mma_commit(BAR_DP_FULL);
             s = s2;
@@ -363,7 +382,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
         const float* dvec = lse2 + 128;
         if (!mbar_wait(BAR_S_FULL, gi & 1, abort_flag, a.status, lim)) { ok = false; break; }
         // the LSE / D slices of this stage arrived with the Q tile
-        if (!mbar_wait(bar_qd_full(s), (gi >> 1) & 1, abort_flag, a.status, lim)) { ok = false; break; }
+        if (!mbar_wait(bar_q_full(s), (gi >> 1) & 1, abort_flag, a.status, lim)) { ok = false; break; }
         tc_fence_after();
         uint32_t pr[64];
         RA_TMEM_LD32(tS, pr);
@@ -446,22 +465,18 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
         ++dq_cnt;
         tc_fence_after();
         const int s = (dq_cnt - 1) & 1;  // the stage that held Q_i, dO_i
-        // read the dQ row 64 columns at a time (register budget), hand the
-        // TMEM columns back after the last read, and stage it: box c, row r,
-        // 16-byte chunk j at r * 128 + ((j ^ (r & 7)) << 4) (128-byte swizzle)
+        constexpr int HALF = D / 2;           // columns per staging round
+        constexpr int BPR = HALF / 32;        // 16 KB boxes per round
+        // round 0: columns [0, HALF) -> dO buffer; box cc, row r, 16-byte
+        // chunk j at r * 128 + ((j ^ (r & 7)) << 4) (128-byte swizzle)
+        {
+          uint32_t v[HALF];
 #pragma unroll
-        for (int c0 = 0; c0 < D; c0 += 64) {
-          uint32_t v[64];
-          RA_TMEM_LD32(T_DP + lane_off + c0, v);
-          RA_TMEM_LD32(T_DP + lane_off + c0 + 32, (v + 32));
+          for (int c = 0; c < HALF; c += 32) RA_TMEM_LD32(T_DP + lane_off + c, (v + c));
           tmem_ld_wait();
-          if (c0 + 64 >= D) {
-            tc_fence_before();
-            mbar_arrive(BAR_DQ_FREE);
-          }
 #pragma unroll
-          for (int cc = 0; cc < 2; ++cc) {
-            uint8_t* box = smem + dq_box<D>(s, c0 / 32 + cc) + r * 128;
+          for (int cc = 0; cc < BPR; ++cc) {
+            uint8_t* box = smem + dq_box<D>(s, cc) + r * 128;
 #pragma unroll
             for (int j = 0; j < 8; ++j)
               *reinterpret_cast<uint4*>(box + ((j ^ (r & 7)) << 4)) =
@@ -470,14 +485,42 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
         }
         fence_proxy_async_smem();
         mbar_arrive(BAR_DQ_STAGED);
-        if (warp == 10 && lane == 0) {
-          if (!mbar_wait(BAR_DQ_STAGED, (dq_cnt - 1) & 1, abort_flag, a.status, lim)) { ok = false; break; }
+        // round 1's columns stay in registers; the TMEM columns go back to the MMA warp
+        uint32_t v1[HALF];
 #pragma unroll
-          for (int c = 0; c < D / 32; ++c)
-            tma_reduce_add_4d(&a.tm_dq, sbase + dq_box<D>(s, c), 32 * c, h, qt * 128, bu.b);
+        for (int c = 0; c < HALF; c += 32) RA_TMEM_LD32(T_DP + lane_off + HALF + c, (v1 + c));
+        tmem_ld_wait();
+        tc_fence_before();
+        mbar_arrive(BAR_DQ_FREE);
+        if (warp == 10 && lane == 0) {
+          if (!mbar_wait(BAR_DQ_STAGED, 0, abort_flag, a.status, lim)) { ok = false; break; }
+#pragma unroll
+          for (int cc = 0; cc < BPR; ++cc)
+            tma_reduce_add_4d(&a.tm_dq, sbase + dq_box<D>(s, cc), 32 * cc, h, qt * 128, bu.b);
           bulk_commit();
-          bulk_wait_read_all();  // the stage may be refilled once the TMA engine has read it
-          mbar_arrive(bar_qd_empty(s));
+          bulk_wait_read_all();
+          mbar_arrive(BAR_DQ_DRAINED);
+        }
+        if (!mbar_wait(BAR_DQ_DRAINED, (dq_cnt - 1) & 1, abort_flag, a.status, lim)) { ok = false; break; }
+        // round 1: columns [HALF, D) into the same buffer
+#pragma unroll
+        for (int cc = 0; cc < BPR; ++cc) {
+          uint8_t* box = smem + dq_box<D>(s, cc) + r * 128;
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            *reinterpret_cast<uint4*>(box + ((j ^ (r & 7)) << 4)) =
+                make_uint4(v1[32 * cc + 4 * j], v1[32 * cc + 4 * j + 1], v1[32 * cc + 4 * j + 2], v1[32 * cc + 4 * j + 3]);
+        }
+        fence_proxy_async_smem();
+        mbar_arrive(BAR_DQ_STAGED);
+        if (warp == 10 && lane == 0) {
+          if (!mbar_wait(BAR_DQ_STAGED, 1, abort_flag, a.status, lim)) { ok = false; break; }
+#pragma unroll
+          for (int cc = 0; cc < BPR; ++cc)
+            tma_reduce_add_4d(&a.tm_dq, sbase + dq_box<D>(s, cc), HALF + 32 * cc, h, qt * 128, bu.b);
+          bulk_commit();
+          bulk_wait_read_all();  // the dO buffer may be refilled once the TMA engine has read it
+          mbar_arrive(bar_do_empty(s));
         }
       }
       if (!ok) break;
