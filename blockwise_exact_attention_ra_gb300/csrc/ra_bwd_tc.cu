@@ -278,11 +278,19 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
       uint32_t qd_cnt = 0, ds_cnt = 0, dq_cnt = 0;
       int k = 0;
       bool ok = true;
-      auto mma_nt = [&](uint32_t dt, uint32_t sa, uint32_t sb) {  // K-major A and B, K = D
+      // descriptors built once: K-major (LBO unused) and MN-major (LBO = the
+      // 16 KB step between 64-column halves) views of each tile
+      const uint64_t dK_k = smem_desc_sw128(sK, 16, 1024), dK_mn = smem_desc_sw128(sK, 16384, 1024);
+      const uint64_t dV_k = smem_desc_sw128(sV, 16, 1024);
+      const uint64_t dS_k = smem_desc_sw128(sDS, 16, 1024), dS_mn = smem_desc_sw128(sDS, 16384, 1024);
+      const uint64_t dQ_k0 = smem_desc_sw128(sbase + L::kQ0, 16, 1024), dQ_mn0 = smem_desc_sw128(sbase + L::kQ0, 16384, 1024);
+      const uint64_t dO_k0 = smem_desc_sw128(sbase + L::kDO0, 16, 1024), dO_mn0 = smem_desc_sw128(sbase + L::kDO0, 16384, 1024);
+      constexpr uint32_t kStageStep = L::kTile >> 4;  // descriptor step between the two stages
+      auto mma_nt = [&](uint32_t dt, uint64_t da, uint64_t db) {  // K-major A and B, K = D
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-          mma_ss(dt, smem_desc_sw128(sa + off, 16, 1024), smem_desc_sw128(sb + off, 16, 1024), id_kq, kk > 0);
+          mma_ss(dt, desc_off(da, off), desc_off(db, off), id_kq, kk > 0);
         }
       };
       auto wait = [&](uint32_t bar, uint32_t par) {
@@ -296,14 +304,14 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
         // prologue: S(0), dP(0)
         uint32_t s = qd_cnt & 1;
         if (!wait(bar_q_full(s), (qd_cnt >> 1) & 1)) break;
-        mma_nt(T_S, sK, sbase + L::kQ0 + s * L::kTile);
+        mma_nt(T_S, dK_k, dQ_k0 + s * kStageStep);
         mma_commit(BAR_S_FULL);
         if (dq_cnt > 0 && !wait(BAR_DQ_FREE, (dq_cnt - 1) & 1)) break;
         if (!wait(bar_do_full(s), (qd_cnt >> 1) & 1)) break;
-        mma_nt(T_DP, sV, sbase + L::kDO0 + s * L::kTile);
+        mma_nt(T_DP, dV_k, dO_k0 + s * kStageStep);
         mma_commit(BAR_DP_FULL);
         for (int it = 0; it < bu.n_iter; ++it) {
-          const uint32_t sQ = sbase + L::kQ0 + s * L::kTile, sDO = sbase + L::kDO0 + s * L::kTile;
+          const uint64_t dQ_mn = dQ_mn0 + s * kStageStep, dO_mn = dO_mn0 + s * kStageStep;
           if (!wait(BAR_DS_FULL, ds_cnt & 1)) break;
           ++ds_cnt;
           if (it == 0 && k > 0 && !wait(BAR_DKV_FREE, (k - 1) & 1)) break;
@@ -311,35 +319,33 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk) {
             const uint32_t pa = T_S + (kk < 4 ? kk * 8 : 64 + (kk - 4) * 8);
-            mma_ts(T_DV, pa, smem_desc_sw128(sDO + kk * 2048, 16384, 1024), id_acc, (it > 0 || kk > 0) ? 1u : 0u);
+            mma_ts(T_DV, pa, desc_off(dO_mn, kk * 2048), id_acc, (it > 0 || kk > 0) ? 1u : 0u);
           }
           const bool has_next = it + 1 < bu.n_iter;
           const uint32_t s2 = (qd_cnt + 1) & 1, par2 = ((qd_cnt + 1) >> 1) & 1;
           if (has_next) {
             if (!wait(bar_q_full(s2), par2)) break;
-            mma_nt(T_S, sK, sbase + L::kQ0 + s2 * L::kTile);
+            mma_nt(T_S, dK_k, dQ_k0 + s2 * kStageStep);
             mma_commit(BAR_S_FULL);
           }
           // dK += dS^T Q_i   (dS^T K-major: key rows of 64-query swizzled halves)
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk) {
             const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-            mma_ss(T_DK, smem_desc_sw128(sDS + off, 16, 1024), smem_desc_sw128(sQ + kk * 2048, 16384, 1024), id_acc,
-                   (it > 0 || kk > 0) ? 1u : 0u);
+            mma_ss(T_DK, desc_off(dS_k, off), desc_off(dQ_mn, kk * 2048), id_acc, (it > 0 || kk > 0) ? 1u : 0u);
           }
           if (PRECISE) {  // + dS_lo^T Q_i, dS_lo^T in TMEM (queries 0-63 at dP columns 0-31, 64-127 at 64-95)
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk) {
               const uint32_t la = T_DP + (kk < 4 ? kk * 8 : 64 + (kk - 4) * 8);
-              mma_ts(T_DK, la, smem_desc_sw128(sQ + kk * 2048, 16384, 1024), id_acc, 1u);
+              mma_ts(T_DK, la, desc_off(dQ_mn, kk * 2048), id_acc, 1u);
             }
           }
           mma_commit(bar_q_empty(s));  // dK was the last reader of Q_i
           // dQ_i = dS K   (the same dS^T tile read MN-major: M = queries)
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk) {
-            mma_ss(T_DP, smem_desc_sw128(sDS + kk * 2048, 16384, 1024), smem_desc_sw128(sK + kk * 2048, 16384, 1024),
-                   id_dq, kk > 0 ? 1u : 0u);
+            mma_ss(T_DP, desc_off(dS_mn, kk * 2048), desc_off(dK_mn, kk * 2048), id_dq, kk > 0 ? 1u : 0u);
           }
           mma_commit(BAR_DQ_FULL);  // dO_i is consumed too; the dQ warps stage dQ_i in its buffer
           ++dq_cnt;
@@ -348,7 +354,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
           if (has_next) {
             if (!wait(BAR_DQ_FREE, (dq_cnt - 1) & 1)) break;
             if (!wait(bar_do_full(s2), par2)) break;
-            mma_nt(T_DP, sV, sbase + L::kDO0 + s2 * L::kTile);
+            mma_nt(T_DP, dV_k, dO_k0 + s2 * kStageStep);
             mma_commit(BAR_DP_FULL);
             s = s2;
           } else {

@@ -245,6 +245,15 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr, uint32_t lbo
   return d;
 }
 
+// The start address occupies the low 14 bits (address >> 4) and shared
+// addresses stay below 256 KB, so a descriptor built once for a tile can be
+// moved by a byte offset with one add (no carry out of the field).  The MMA
+// warp shares its SM sub-partition with busy warps; rebuilding both 64-bit
+// descriptors for every MMA made issue, not the tensor core, the limit.
+__device__ __forceinline__ uint64_t desc_off(uint64_t d, uint32_t byte_off) {
+  return d + (uint64_t)(byte_off >> 4);
+}
+
 // Instruction descriptor for kind::f16: D fp32, A/B type (0 = fp16,
 // 1 = bf16), operand majorness (0 = K-major, 1 = MN-major), N >> 3 at bit 17,
 // M >> 4 at bit 24.

@@ -285,28 +285,29 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
       uint32_t p_cnt[2] = {0, 0};
       int k = 0;
       bool ok = true;
+      // descriptors built once; each MMA advances one with a single add
+      const uint64_t dQ_k[2] = {smem_desc_sw128(sbase + L::kQA, 16, 1024), smem_desc_sw128(sbase + L::kQB, 16, 1024)};
+      const uint64_t dKV_k0 = smem_desc_sw128(sbase + L::kStage0, 16, 1024);
+      const uint64_t dKV_mn0 = smem_desc_sw128(sbase + L::kStage0, 16384, 1024);
+      constexpr uint32_t kStageStep = L::kTileBytes >> 4;
       auto issue_s = [&](int x, uint32_t kstage) {
-        const uint32_t qa = sbase + (x == 0 ? L::kQA : L::kQB);
-        const uint32_t kb = sbase + L::kStage0 + kstage * L::kTileBytes;
+        const uint64_t da = dQ_k[x], db = dKV_k0 + kstage * kStageStep;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-          mma_ss(tS[x], smem_desc_sw128(qa + off, 16, 1024), smem_desc_sw128(kb + off, 16, 1024),
-                 idesc_qk, kk > 0);
+          mma_ss(tS[x], desc_off(da, off), desc_off(db, off), idesc_qk, kk > 0);
         }
         mma_commit(bar_s_full(x));
       };
       auto issue_pv = [&](int x, uint32_t vstage, bool accumulate) {
-        const uint32_t vb = sbase + L::kStage0 + vstage * L::kTileBytes;
+        const uint64_t db = dKV_mn0 + vstage * kStageStep;
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
-          mma_ts(tO[x], tS[x] + kk * 8, smem_desc_sw128(vb + kk * 2048, 16384, 1024), idesc_pv,
-                 (accumulate || kk > 0) ? 1u : 0u);
+          mma_ts(tO[x], tS[x] + kk * 8, desc_off(db, kk * 2048), idesc_pv, (accumulate || kk > 0) ? 1u : 0u);
         }
         if (PRECISE) {  // + P_lo V
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk)
-            mma_ts(tO[x], tS[x] + 64 + kk * 8, smem_desc_sw128(vb + kk * 2048, 16384, 1024), idesc_pv, 1u);
+          for (int kk = 0; kk < 8; ++kk) mma_ts(tO[x], tS[x] + 64 + kk * 8, desc_off(db, kk * 2048), idesc_pv, 1u);
         }
       };
       for (int u = blockIdx.x; u < a.num_units && ok; u += gridDim.x) {
