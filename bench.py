@@ -304,6 +304,31 @@ def run_ours(args, ws, rank, local):
             "traffic": kernel_traffic(dom),
             "peak_source": peaks["source"] + ", bf16 sustained (dense fp16 runs at the bf16 rate)"}
 
+    # the striped (load-balanced) causal layout on the same tensors: same
+    # algorithmic work, every virtual host with an equal share
+    striped = None
+    if not args.no_striped:
+        def step_striped(ev=None):
+            ra.ra_ring_fwd(q, k, v, P, True, scale, o, lse, wsf, stream, striped=True)
+            if ev is not None:
+                ev.record(stream)
+            ra.ra_ring_bwd(q, k, v, o, do, lse, P, True, scale, dq, dk, dv, wsb, stream, striped=True)
+        for _ in range(args.warmup):
+            step_striped()
+        torch.cuda.synchronize(dev)
+        sa = [torch.cuda.Event(enable_timing=True) for _ in range(3 * args.steps)]
+        for s_ in range(args.steps):
+            sa[3 * s_].record(stream)
+            step_striped(sa[3 * s_ + 1])
+            sa[3 * s_ + 2].record(stream)
+        torch.cuda.synchronize(dev)
+        ra.ra_sync_status(stream)
+        f_ms = sum(sa[3 * i].elapsed_time(sa[3 * i + 1]) for i in range(args.steps)) / args.steps
+        b_ms = sum(sa[3 * i + 1].elapsed_time(sa[3 * i + 2]) for i in range(args.steps)) / args.steps
+        striped = {"layout": "striped rows (host i local row l = position l*P + i)",
+                   "tflops": (fwd_fl + bwd_fl) / ((f_ms + b_ms) * 1e-3) / 1e12,
+                   "fwd_tflops": fwd_fl / (f_ms * 1e-3) / 1e12, "bwd_tflops": bwd_fl / (b_ms * 1e-3) / 1e12}
+
     # end to end through the public API with pinned host buffers
     e2e = None
     if not args.no_e2e:
@@ -364,7 +389,7 @@ def run_ours(args, ws, rank, local):
             "pct_of_peak": value / ws / peaks["sustained"],
             "fwd_ms": fwd_ms, "bwd_ms": bwd_ms,
             "fwd_tflops": fwd_fl / (fwd_ms * 1e-3) / 1e12, "bwd_tflops": bwd_fl / (bwd_ms * 1e-3) / 1e12,
-            "kernels": kern, "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
+            "kernels": kern, "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "striped": striped,
             "gpu_launches": launches, "clocks": clk,
         }
         print(json.dumps(line), flush=True)
@@ -380,8 +405,9 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-striped", action="store_true", help="skip the striped-layout measurement")
     ap.add_argument("--cpu-rows", type=int, default=3072)
-    ap.add_argument("--ref-rows", type=int, default=48)
+    ap.add_argument("--ref-rows", type=int, default=1024)
     ap.add_argument("--N", type=int, default=None, help="override N (profiling on a smaller case)")
     ap.add_argument("--heads", type=int, default=None, help="override the head count (profiling)")
     args = ap.parse_args()

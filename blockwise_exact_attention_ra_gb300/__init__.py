@@ -23,11 +23,11 @@ __all__ = [
     "ra_sync_status", "ra_last_error", "ra_launch_count", "ra_selftest_timeout",
     "ra_kernel_timing", "ra_kernel_timing_read",
     "ring_attention_fwd", "ring_attention_bwd", "RA_F32", "RA_BF16", "RA_F16",
-    "RA_CAUSAL", "RA_PRECISE",
+    "RA_CAUSAL", "RA_PRECISE", "RA_STRIPED",
 ]
 
 RA_F32, RA_BF16, RA_F16 = 0, 1, 2
-RA_CAUSAL, RA_PRECISE = 1, 2
+RA_CAUSAL, RA_PRECISE, RA_STRIPED = 1, 2, 4
 STATUS = {0: "RA_OK", 1: "RA_ERR_INVALID_ARG", 2: "RA_ERR_UNSUPPORTED", 3: "RA_ERR_CUDA",
           4: "RA_ERR_RANGE", 5: "RA_ERR_TIMEOUT"}
 _DTYPES = {torch.float32: RA_F32, torch.bfloat16: RA_BF16, torch.float16: RA_F16}
@@ -196,22 +196,23 @@ def ra_ring_fwd_workspace_bytes(dtype, shape, P):
     return int(lib.ra_ring_fwd_workspace_bytes(dtype, shape, P))
 
 
-def ra_ring_fwd(q, k, v, P, causal, scale, o, lse, workspace=None, stream=None, precise=False):
+def ra_ring_fwd(q, k, v, P, causal, scale, o, lse, workspace=None, stream=None, precise=False,
+                striped=False):
     shape = shape_of(q, k)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
-    _check(lib.ra_ring_fwd(_ptr(q), _ptr(k), _ptr(v), _dt(q), shape, int(P), _flags(causal, precise),
+    _check(lib.ra_ring_fwd(_ptr(q), _ptr(k), _ptr(v), _dt(q), shape, int(P), _flags(causal, precise, striped),
                            float(scale), _ptr(o), _dt(o), _ptr(lse), _ptr(workspace), ws_bytes,
                            _stream(stream)))
 
 
-def ra_ring_fwd_noalloc(q, k, v, P, causal, scale, o, lse, stream=None, precise=False):
+def ra_ring_fwd_noalloc(q, k, v, P, causal, scale, o, lse, stream=None, precise=False, striped=False):
     """ra_ring_fwd without a workspace, for callers that cannot allocate device
     memory: the library's own 32 MiB per-device scratch buffer is used instead
     (shapes needing more are rejected).  Calls that overlap on the GPU race on
     that buffer."""
     shape = shape_of(q, k)
     _check(lib.ra_ring_fwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _dt(q), shape, int(P),
-                                   _flags(causal, precise), float(scale), _ptr(o), _dt(o),
+                                   _flags(causal, precise, striped), float(scale), _ptr(o), _dt(o),
                                    _ptr(lse), _stream(stream)))
 
 
@@ -220,17 +221,17 @@ def ra_ring_bwd_workspace_bytes(dtype, grad_dtype, shape, P):
 
 
 def ra_ring_bwd(q, k, v, o, dO, lse, P, causal, scale, dq, dk, dv, workspace, stream=None,
-                precise=False):
+                precise=False, striped=False):
     shape = shape_of(q, k)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _check(lib.ra_ring_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _dt(o), _ptr(dO), _ptr(lse),
-                           _dt(q), shape, int(P), _flags(causal, precise), float(scale), _ptr(dq),
+                           _dt(q), shape, int(P), _flags(causal, precise, striped), float(scale), _ptr(dq),
                            _ptr(dk), _ptr(dv), _dt(dq), _ptr(workspace), ws_bytes,
                            _stream(stream)))
 
 
-def _flags(causal, precise):
-    return (RA_CAUSAL if causal else 0) | (RA_PRECISE if precise else 0)
+def _flags(causal, precise, striped=False):
+    return (RA_CAUSAL if causal else 0) | (RA_PRECISE if precise else 0) | (RA_STRIPED if striped else 0)
 
 
 def _workspace(nbytes, device):
@@ -238,7 +239,7 @@ def _workspace(nbytes, device):
 
 
 def ring_attention_fwd(q, k, v, P, causal=True, scale=None, o_dtype=torch.float32,
-                       stream=None, precise=False):
+                       stream=None, precise=False, striped=False):
     """Allocate O [B,N,Hq,d] (o_dtype) and LSE [B,Hq,N] fp32 and run the ring forward."""
     if scale is None:
         scale = q.shape[-1] ** -0.5
@@ -246,12 +247,12 @@ def ring_attention_fwd(q, k, v, P, causal=True, scale=None, o_dtype=torch.float3
     o = torch.empty(B, N, Hq, d, dtype=o_dtype, device=q.device)
     lse = torch.empty(B, Hq, N, dtype=torch.float32, device=q.device)
     ws = _workspace(ra_ring_fwd_workspace_bytes(_dt(q), shape_of(q, k), P), q.device)
-    ra_ring_fwd(q, k, v, P, causal, scale, o, lse, ws, stream, precise)
+    ra_ring_fwd(q, k, v, P, causal, scale, o, lse, ws, stream, precise, striped)
     return o, lse
 
 
 def ring_attention_bwd(q, k, v, o, lse, dO, P, causal=True, scale=None,
-                       grad_dtype=torch.float32, stream=None, precise=False):
+                       grad_dtype=torch.float32, stream=None, precise=False, striped=False):
     """Allocate dQ, dK, dV (grad_dtype) and workspace and run the ring backward."""
     if scale is None:
         scale = q.shape[-1] ** -0.5
@@ -260,5 +261,5 @@ def ring_attention_bwd(q, k, v, o, lse, dO, P, causal=True, scale=None,
     dv = torch.empty(v.shape, dtype=grad_dtype, device=q.device)
     ws = _workspace(ra_ring_bwd_workspace_bytes(_dt(q), _DTYPES[grad_dtype], shape_of(q, k), P),
                     q.device)
-    ra_ring_bwd(q, k, v, o, dO, lse, P, causal, scale, dq, dk, dv, ws, stream, precise)
+    ra_ring_bwd(q, k, v, o, dO, lse, P, causal, scale, dq, dk, dv, ws, stream, precise, striped)
     return dq, dk, dv

@@ -475,7 +475,9 @@ int ra_ring_fwd(const void* q, const void* k, const void* v, ra_dtype dtype, ra_
                 int P, int flags, float scale, void* o, ra_dtype o_dtype, float* lse,
                 void* workspace, size_t ws_bytes, void* stream) {
   const int causal = (flags & RA_CAUSAL) != 0, precise = (flags & RA_PRECISE) != 0;
-  if (flags & ~(RA_CAUSAL | RA_PRECISE)) return fail(RA_ERR_INVALID_ARG, "unknown flag bits 0x%x", flags);
+  const int striped = causal && (flags & RA_STRIPED) != 0;
+  if (flags & ~(RA_CAUSAL | RA_PRECISE | RA_STRIPED))
+    return fail(RA_ERR_INVALID_ARG, "unknown flag bits 0x%x", flags);
   Shape s;
   int rc;
   if ((rc = check_shape(shape, &s))) return rc;
@@ -498,7 +500,7 @@ int ra_ring_fwd(const void* q, const void* k, const void* v, ra_dtype dtype, ra_
     a.B = s.B; a.Nq = s.Nq; a.Nkv = s.Nkv; a.Hq = s.Hq; a.Hkv = s.Hkv; a.d = s.d;
     a.q_bs = s.q_bs; a.kv_bs = s.kv_bs;
     a.scale = scale; a.causal = causal;
-    a.P = P; a.S = s.Nq / P;
+    a.P = P; a.S = s.Nq / P; a.striped = striped;
     a.o_out = o; a.o_dtype = o_dtype; a.o_bs = s.q_bs; a.lse = lse;
     TimedLaunch tl(RA_KERNEL_FWD_F32, cs);
     cudaError_t e = launch_simt_fwd(a, cs);
@@ -528,7 +530,7 @@ int ra_ring_fwd(const void* q, const void* k, const void* v, ra_dtype dtype, ra_
   a.B = s.B; a.Nq = s.Nq; a.Nkv = s.Nkv; a.Hq = s.Hq; a.Hkv = s.Hkv; a.d = s.d;
   a.scale_log2 = scale * 1.4426950408889634f;
   a.causal = causal;
-  a.ring_P = P; a.ring_S = s.Nq / P; a.mode = 0; a.precise = precise;
+  a.ring_P = P; a.ring_S = s.Nq / P; a.mode = 0; a.precise = precise; a.striped = striped;
   a.o_out = o; a.o_dtype = o_dtype; a.o_bs = s.q_bs; a.lse = lse;
   a.status = st;
   a.wait_limit_ns = wait_limit_ns();
@@ -576,7 +578,9 @@ int ra_ring_bwd(const void* q, const void* k, const void* v, const void* o, ra_d
                 int flags, float scale, void* dq, void* dk, void* dv, ra_dtype grad_dtype,
                 void* workspace, size_t ws_bytes, void* stream) {
   const int causal = (flags & RA_CAUSAL) != 0, precise = (flags & RA_PRECISE) != 0;
-  if (flags & ~(RA_CAUSAL | RA_PRECISE)) return fail(RA_ERR_INVALID_ARG, "unknown flag bits 0x%x", flags);
+  const int striped = causal && (flags & RA_STRIPED) != 0;
+  if (flags & ~(RA_CAUSAL | RA_PRECISE | RA_STRIPED))
+    return fail(RA_ERR_INVALID_ARG, "unknown flag bits 0x%x", flags);
   Shape s;
   int rc;
   if ((rc = check_shape(shape, &s))) return rc;
@@ -613,7 +617,7 @@ int ra_ring_bwd(const void* q, const void* k, const void* v, const void* o, ra_d
     a.B = s.B; a.N = s.Nq; a.Hq = s.Hq; a.Hkv = s.Hkv; a.d = s.d;
     a.q_bs = s.q_bs; a.kv_bs = s.kv_bs;
     a.scale = scale; a.causal = causal;
-    a.P = P; a.S = s.Nq / P;
+    a.P = P; a.S = s.Nq / P; a.striped = striped;
     a.dq = dq; a.dk = dk; a.dv = dv; a.grad_dtype = grad_dtype;
     {
       TimedLaunch tl(RA_KERNEL_BWD_F32, cs);
@@ -653,7 +657,7 @@ int ra_ring_bwd(const void* q, const void* k, const void* v, const void* o, ra_d
   a.scale = scale;
   a.scale_log2 = scale * 1.4426950408889634f;
   a.causal = causal;
-  a.ring_P = P; a.ring_S = s.Nq / P; a.precise = precise;
+  a.ring_P = P; a.ring_S = s.Nq / P; a.precise = precise; a.striped = striped;
   a.lse = lse2; a.Dvec = Dv; a.dq_acc = dq_acc;
   a.dk = dk; a.dv = dv; a.grad_dtype = grad_dtype; a.kv_bs = s.kv_bs;
   a.status = st;

@@ -79,6 +79,7 @@ struct BwdUnit {
   int b, g, jt;
   int count;  // query tiles per head
   int n_iter; // count * group
+  int host, tk, per_block;  // striped layouts: key host, local key tile, query tiles per block
 };
 
 // Units are ordered head-major: every resident CTA works on the same
@@ -86,6 +87,7 @@ struct BwdUnit {
 // accumulator rows they sweep stay in L2 (one head of them is ~128 MB at
 // N = 131072).  Within a head the earliest key tiles come first: under a
 // causal mask they have the most work.
+template <bool STRIPED>
 __device__ __forceinline__ BwdUnit bwd_unit(const TcBwdArgs& a, int u) {
   BwdUnit r;
   const int nT = a.N / 128;
@@ -93,17 +95,37 @@ __device__ __forceinline__ BwdUnit bwd_unit(const TcBwdArgs& a, int u) {
   r.jt = u % nT;
   r.b = bg / a.Hkv;
   r.g = bg % a.Hkv;
+  if (STRIPED) {
+    // striped: local key tile tk meets local query tiles tk..T-1 of every host;
+    // smallest local tiles (most work) first, across hosts
+    const int T = a.ring_S / 128;
+    const int idx = u % nT;
+    r.tk = idx / a.ring_P;
+    r.host = idx % a.ring_P;
+    r.jt = r.host * T + r.tk;
+    r.per_block = T - r.tk;
+    r.count = a.ring_P * r.per_block;
+    r.n_iter = r.count * (a.Hq / a.Hkv);
+    return r;
+  }
   r.count = a.causal ? nT - r.jt : nT;
   r.n_iter = r.count * (a.Hq / a.Hkv);
   return r;
 }
 
 // Query head and query tile of iteration it, in ring order.
+template <bool STRIPED>
 __device__ __forceinline__ void bwd_iter(const TcBwdArgs& a, const BwdUnit& u, int it, int* h,
                                          int* qt) {
   const int group = a.Hq / a.Hkv;
   const int hh = it / u.count, k = it % u.count;
   *h = u.g * group + hh;
+  if (STRIPED) {  // query hosts (j + s) mod P, local tiles tk..T-1 in each
+    const int s = k / u.per_block;
+    const int qh = (u.host + s) % a.ring_P;
+    *qt = qh * (a.ring_S / 128) + u.tk + (k - s * u.per_block);
+    return;
+  }
   if (a.causal) {
     *qt = u.jt + k;
   } else {
@@ -146,7 +168,7 @@ __device__ __forceinline__ uint32_t dq_box(int s, int cc) {
   return L::kDO0 + s * L::kTile + cc * 16384;
 }
 
-template <int D, bool PRECISE>
+template <int D, bool PRECISE, bool STRIPED>
 __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_constant__ TcBwdArgs a) {
   using L = BwdSmem<D>;
   extern __shared__ __align__(1024) uint8_t smem[];
@@ -223,7 +245,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
       int k = 0;
       bool ok = true;
       for (int u = blockIdx.x; u < a.num_units && ok; u += gridDim.x, ++k) {
-        const BwdUnit bu = bwd_unit(a, u);
+        const BwdUnit bu = bwd_unit<STRIPED>(a, u);
         if (!mbar_wait(BAR_KV_EMPTY, (k & 1) ^ 1, abort_flag, a.status, lim)) { ok = false; break; }
         mbar_arrive_expect_tx(BAR_KV_FULL, 2 * L::kTile);
 #pragma unroll
@@ -233,7 +255,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
         }
         for (int it = 0; it < bu.n_iter; ++it) {
           int h, qt;
-          bwd_iter(a, bu, it, &h, &qt);
+          bwd_iter<STRIPED>(a, bu, it, &h, &qt);
           const int s = qd_cnt & 1;
           const uint32_t par = ((qd_cnt >> 1) & 1) ^ 1;
           if (!mbar_wait(bar_q_empty(s), par, abort_flag, a.status, lim)) { ok = false; break; }
@@ -299,7 +321,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
         return ok;
       };
       for (int u = blockIdx.x; u < a.num_units && ok; u += gridDim.x, ++k) {
-        const BwdUnit bu = bwd_unit(a, u);
+        const BwdUnit bu = bwd_unit<STRIPED>(a, u);
         if (!wait(BAR_KV_FULL, k & 1)) break;
         // prologue: S(0), dP(0)
         uint32_t s = qd_cnt & 1;
@@ -379,10 +401,10 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
     uint32_t gi = 0;  // iterations done by this CTA (all units)
     bool ok = true;
     for (int u = blockIdx.x; u < a.num_units && ok; u += gridDim.x) {
-      const BwdUnit bu = bwd_unit(a, u);
+      const BwdUnit bu = bwd_unit<STRIPED>(a, u);
       for (int it = 0; it < bu.n_iter; ++it, ++gi) {
         int h, qt;
-        bwd_iter(a, bu, it, &h, &qt);
+        bwd_iter<STRIPED>(a, bu, it, &h, &qt);
         const int s = gi & 1;
         const float* lse2 = reinterpret_cast<const float*>(smem + L::kVec0 + s * 1024) + half * 64;
         const float* dvec = lse2 + 128;
@@ -394,7 +416,19 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
         RA_TMEM_LD32(tS, pr);
         RA_TMEM_LD32(tS + 32, (pr + 32));
         tmem_ld_wait();
-        const bool diag = a.causal && qt == bu.jt;
+        // causal masks: the diagonal tile of a contiguous layout (query column
+        // c visible to key row r iff c >= r); for a striped layout the same
+        // local tile of any host pair, strict (c > r) when the key's host
+        // comes after the query's
+        bool diag;
+        int strict = 0;
+        if (STRIPED) {
+          const int T_local = a.ring_S / 128;
+          diag = qt % T_local == bu.tk;
+          strict = bu.host > qt / T_local ? 1 : 0;
+        } else {
+          diag = a.causal && qt == bu.jt;
+        }
         // P^T = exp2(S^T * scale*log2e - LSE*log2e); query column c visible iff c >= key row
 #pragma unroll
         for (int c = 0; c < 64; c += 4) {
@@ -403,7 +437,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
 #pragma unroll
           for (int u4 = 0; u4 < 4; ++u4) {
             float p = ex2_approx(fmaf(__uint_as_float(pr[c + u4]), sl2, -lv[u4]));
-            if (diag && half * 64 + c + u4 < r) p = 0.f;
+            if (diag && half * 64 + c + u4 < r + strict) p = 0.f;
             pr[c + u4] = __float_as_uint(p);
           }
         }
@@ -463,10 +497,10 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
     int k = 0;
     bool ok = true;
     for (int u = blockIdx.x; u < a.num_units && ok; u += gridDim.x, ++k) {
-      const BwdUnit bu = bwd_unit(a, u);
+      const BwdUnit bu = bwd_unit<STRIPED>(a, u);
       for (int it = 0; it < bu.n_iter; ++it) {
         int h, qt;
-        bwd_iter(a, bu, it, &h, &qt);
+        bwd_iter<STRIPED>(a, bu, it, &h, &qt);
         if (!mbar_wait(BAR_DQ_FULL, dq_cnt & 1, abort_flag, a.status, lim)) { ok = false; break; }
         ++dq_cnt;
         tc_fence_after();
@@ -593,14 +627,23 @@ cudaError_t launch_tc_bwd(TcBwdArgs& a, int num_sms, cudaStream_t st) {
     kernel<<<grid, kThreads, smem, st>>>(a);
     return cudaSuccess;
   };
-  if (a.d == 128)
-    e = a.precise ? run(tc_bwd_kernel<128, true>, BwdSmem<128>::kBytes)
-                  : run(tc_bwd_kernel<128, false>, BwdSmem<128>::kBytes);
-  else if (a.d == 64)
-    e = a.precise ? run(tc_bwd_kernel<64, true>, BwdSmem<64>::kBytes)
-                  : run(tc_bwd_kernel<64, false>, BwdSmem<64>::kBytes);
-  else
+  if (a.d == 128) {
+    if (a.striped)
+      e = a.precise ? run(tc_bwd_kernel<128, true, true>, BwdSmem<128>::kBytes)
+                    : run(tc_bwd_kernel<128, false, true>, BwdSmem<128>::kBytes);
+    else
+      e = a.precise ? run(tc_bwd_kernel<128, true, false>, BwdSmem<128>::kBytes)
+                    : run(tc_bwd_kernel<128, false, false>, BwdSmem<128>::kBytes);
+  } else if (a.d == 64) {
+    if (a.striped)
+      e = a.precise ? run(tc_bwd_kernel<64, true, true>, BwdSmem<64>::kBytes)
+                    : run(tc_bwd_kernel<64, false, true>, BwdSmem<64>::kBytes);
+    else
+      e = a.precise ? run(tc_bwd_kernel<64, true, false>, BwdSmem<64>::kBytes)
+                    : run(tc_bwd_kernel<64, false, false>, BwdSmem<64>::kBytes);
+  } else {
     return cudaErrorInvalidValue;
+  }
   if (e != cudaSuccess) return e;
   count_launch();
   return cudaGetLastError();

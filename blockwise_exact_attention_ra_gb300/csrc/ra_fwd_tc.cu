@@ -72,19 +72,46 @@ struct UnitInfo {
   int qa_row0;    // tensor row of tile A (tile B = qa_row0 + 128)
   int has_b;
   int n_iter;     // key/value tiles visited
-  int start[2];   // first iteration at which tile A / B is active
+  int start[2];   // contiguous layouts: first iteration at which tile A / B is active
   long long qpos0[2];  // global position of row 0 of tile A / B
-  // key/value tile at iteration it:
+  // key/value tile at iteration it (contiguous layouts):
   //   kt = ring_noncausal ? (kt0 - it) mod nkt : kt0 - it
   int kt0;
   int nkt;
   int wrap;
+  // striped causal ring: host `host` visits blocks (host - s) mod P, and in
+  // each block the local tiles lead, lead-1, ..., 0 (L = lead + 1 per block)
+  int striped, host, P, T, L, tq[2];
 };
 
-__device__ __forceinline__ int kt_at(const UnitInfo& u, int it) {
+// Key/value tile of iteration it: global tile kt, and for striped layouts the
+// local tile tk and the block j it belongs to.
+__device__ __forceinline__ int kt_at(const UnitInfo& u, int it, int* tk = nullptr, int* blk = nullptr) {
+  if (u.striped) {
+    const int s = it / u.L;
+    const int t = u.kt0 - (it - s * u.L);
+    int j = u.host - s;
+    if (j < 0) j += u.P;
+    if (tk) *tk = t;
+    if (blk) *blk = j;
+    return j * u.T + t;
+  }
   int kt = u.kt0 - it;
   if (u.wrap && kt < 0) kt += u.nkt;
   return kt;
+}
+
+// Does query tile x (0 = A, 1 = B) take part in iteration it?
+__device__ __forceinline__ bool active(const UnitInfo& u, int x, int it) {
+  if (u.striped) {
+    if (x == 1) return u.has_b;
+    return u.kt0 - it % u.L <= u.tq[0];
+  }
+  return it >= u.start[x];
+}
+
+__device__ __forceinline__ bool ever_active(const UnitInfo& u, int x) {
+  return u.striped ? (x == 0 || u.has_b) : u.start[x] < u.n_iter;
 }
 
 // Last key/value tile with at least one key visible to some row of a query
@@ -118,6 +145,31 @@ __device__ __forceinline__ UnitInfo unit_info(const TcFwdArgs& a, int u) {
   r.g = r.h / (a.Hq / a.Hkv);
   const int nkt = (a.Nkv + 127) / 128;
   r.nkt = nkt;
+  r.striped = 0;
+  if (a.ring_P > 0 && a.striped) {
+    // striped: the row of a host's local row l holds position l * P + host; every
+    // host has the same work, heaviest local pairs first
+    const int T = a.ring_S / 128;
+    const int pph = (T + 1) / 2;
+    const int lp = pph - 1 - pidx_desc / a.ring_P;
+    const int host = pidx_desc % a.ring_P;
+    r.qa_row0 = host * a.ring_S + lp * 256;
+    r.has_b = (2 * lp + 1) < T;
+    r.qpos0[0] = r.qa_row0;  // unused for striped masks
+    r.qpos0[1] = r.qa_row0 + 128;
+    r.striped = 1;
+    r.host = host;
+    r.P = a.ring_P;
+    r.T = T;
+    r.tq[0] = 2 * lp;
+    r.tq[1] = 2 * lp + 1;
+    r.kt0 = r.has_b ? r.tq[1] : r.tq[0];  // lead local tile
+    r.L = r.kt0 + 1;
+    r.n_iter = a.ring_P * r.L;
+    r.wrap = 0;
+    r.start[0] = r.start[1] = 0;
+    return r;
+  }
   if (a.ring_P > 0) {
     const int T = a.ring_S / 128;
     const int pph = (T + 1) / 2;
@@ -248,7 +300,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
                         ui.qa_row0 + 128, ui.b, pol_q);
         }
         for (int it = 0; it < ui.n_iter && ok; ++it) {
-          const int kt = kt_at(ui, it);
+          int tk = 0, blk = 0;
+        const int kt = kt_at(ui, it, &tk, &blk);
 #pragma unroll
           for (int kv = 0; kv < 2; ++kv) {  // K then V
             const int s = L_cnt % kStages;
@@ -321,7 +374,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
         if (!mbar_wait(bar_kv_full(sk), (L_cnt / kStages) & 1, abort_flag, a.status, lim)) { ok = false; break; }
         tc_fence_after();
         for (int x = 0; x < 2; ++x)
-          if (0 >= ui.start[x]) issue_s(x, sk);
+          if (active(ui, x, 0)) issue_s(x, sk);
         mma_commit(bar_kv_empty(sk));
         ++L_cnt;
         bool first_pv[2] = {a.mode == 0, a.mode == 0};
@@ -338,7 +391,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
           }
           tc_fence_after();
           for (int x = 0; x < 2 && ok; ++x) {
-            if (it >= ui.start[x]) {
+            if (active(ui, x, it)) {
               if (!mbar_wait(bar_p_full(x), p_cnt[x] & 1, abort_flag, a.status, lim)) { ok = false; break; }
               ++p_cnt[x];
               tc_fence_after();
@@ -346,7 +399,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
               first_pv[x] = false;
               if (!has_next) mma_commit(bar_o_full(x));
             }
-            if (has_next && it + 1 >= ui.start[x]) issue_s(x, sk2);
+            if (has_next && active(ui, x, it + 1)) issue_s(x, sk2);
           }
           if (!ok) break;
           mma_commit(bar_kv_empty(sv));
@@ -372,7 +425,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
     bool ok = true;
     for (int u = blockIdx.x; u < a.num_units && ok; u += gridDim.x) {
       const UnitInfo ui = unit_info(a, u);
-      if (ui.start[x] >= ui.n_iter) continue;  // this tile sees no key in this unit
+      if (!ever_active(ui, x)) continue;  // this tile sees no key in this unit
       const int row = ui.qa_row0 + x * 128 + r;  // tensor row
       const bool row_ok = row < a.Nq;
       const long long qpos = ui.qpos0[x] + r;
@@ -402,20 +455,31 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
         }
       }
       bool o_valid = (a.mode == 1);  // O_X holds a state that must be rescaled
-      for (int it = ui.start[x]; it < ui.n_iter; ++it) {
+      for (int it = ui.striped ? 0 : ui.start[x]; it < ui.n_iter; ++it) {
+        if (!active(ui, x, it)) continue;
         if (!mbar_wait(bar_s_full(x), s_cnt & 1, abort_flag, a.status, lim)) { ok = false; break; }
         ++s_cnt;
         tc_fence_after();
-        const int kt = kt_at(ui, it);
+        int tk = 0, blk = 0;
+        const int kt = kt_at(ui, it, &tk, &blk);
         uint32_t sr[128];
 #pragma unroll
         for (int c = 0; c < 128; c += 32) RA_TMEM_LD32(tS + c, (sr + c));
         tmem_ld_wait();
         // element masks: causal diagonal tiles and the ragged end of the keys
         const long long kvpos0 = a.kv_off + (long long)kt * 128;
-        const bool need_mask = (a.causal && kvpos0 + 127 > ui.qpos0[x]) || (kt * 128 + 128 > a.Nkv);
+        bool need_mask;
+        long long lim_c;  // column c of the tile is visible iff c <= lim_c
+        if (ui.striped) {
+          // same local tile: key row c sees query row r iff c < r, or c == r and
+          // the key's host is not after the query's
+          need_mask = tk == ui.tq[x];
+          lim_c = r - (blk > ui.host ? 1 : 0);
+        } else {
+          need_mask = (a.causal && kvpos0 + 127 > ui.qpos0[x]) || (kt * 128 + 128 > a.Nkv);
+          lim_c = a.causal ? qpos - kvpos0 : 127;
+        }
         if (need_mask) {
-          const long long lim_c = a.causal ? qpos - kvpos0 : 127;  // visible iff c <= lim_c
           const int nvalid = a.Nkv - kt * 128;
 #pragma unroll
           for (int c = 0; c < 128; ++c)

@@ -31,6 +31,7 @@ struct SimtFwdArgs {
   int causal;
   long long q_off, kv_off;  // block mode: global positions of row 0
   int P, S;                 // ring mode: P hosts of S rows; P == 0 -> block mode
+  int striped;              // ring mode, causal: rows in striped order (position l*P + host)
   float* o_acc;             // block mode state (read + written)
   float* m_acc;
   float* l_acc;
@@ -52,6 +53,7 @@ struct SimtBwdArgs {
   float scale;
   int causal;
   int P, S;
+  int striped;
   void* dq;
   void* dk;
   void* dv;
@@ -102,6 +104,7 @@ struct TcFwdArgs {
   int causal;
   long long q_off, kv_off;
   int ring_P, ring_S;  // ring mode when ring_P > 0 (Nq == Nkv == P*S, S % 128 == 0)
+  int striped;         // ring mode, causal: rows are in striped order (position l*P + host)
   // outputs
   int mode;         // 0: ring (finalise), 1: block (read/write state)
   float* o_acc;     // block mode: [B, Nq, Hq, d] fp32
@@ -129,6 +132,7 @@ struct TcBwdArgs {
   int causal;
   int precise;  // two-term fp16 dS in the dK product
   int ring_P, ring_S;
+  int striped;  // causal, rows in striped order (position l*P + host)
   const float* lse;   // [B, Hq, N], multiplied by log2(e)
   const float* Dvec;  // [B, Hq, N]
   float* dq_acc;      // packed fp32 [B, N, Hq, d], pre-zeroed, reduce-added

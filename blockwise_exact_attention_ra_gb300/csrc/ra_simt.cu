@@ -109,10 +109,16 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32)
     const int hi = i / a.S;
     for (int s = 0; s < a.P; ++s) {
       const int blk = (hi - s + a.P) % a.P;
-      if (a.causal && blk > hi) continue;
       const int kbeg = blk * a.S;
       int kend = kbeg + a.S;
-      if (a.causal) kend = min(kend, i + 1);
+      if (a.causal && a.striped) {
+        // striped rows: local key row lk is visible iff lk < li, or lk == li
+        // and the key's host is not after the query's
+        kend = kbeg + (i - hi * a.S) + 1 - (blk > hi ? 1 : 0);
+      } else if (a.causal) {
+        if (blk > hi) continue;
+        kend = min(kend, i + 1);
+      }
       simt_fwd_range<DPL>(q_sh[w], kbase, vbase, kv_row_stride, kbeg, kend, a.scale, m, l,
                           o);
     }
@@ -174,10 +180,14 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32) simt_bwd_dq_kernel(const 
   const int hi = i / a.S;
   for (int s = 0; s < a.P; ++s) {
     const int blk = (hi - s + a.P) % a.P;
-    if (a.causal && blk > hi) continue;
     const int kbeg = blk * a.S;
     int kend = kbeg + a.S;
-    if (a.causal) kend = min(kend, i + 1);
+    if (a.causal && a.striped) {
+      kend = kbeg + (i - hi * a.S) + 1 - (blk > hi ? 1 : 0);
+    } else if (a.causal) {
+      if (blk > hi) continue;
+      kend = min(kend, i + 1);
+    }
     for (int c = kbeg; c < kend; c += 32) {
       const int j = c + lane;
       float ds = 0.f;
@@ -240,10 +250,16 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32) simt_bwd_dkdv_kernel(cons
     const long long sbase = ((long long)b * a.Hq + h) * a.N;
     for (int s = 0; s < a.P; ++s) {
       const int host = (hj + s) % a.P;
-      if (a.causal && host < hj) continue;
       int qbeg = host * a.S;
       const int qend = qbeg + a.S;
-      if (a.causal) qbeg = max(qbeg, j);
+      if (a.causal && a.striped) {
+        // striped rows: local query row lq sees this key iff lq > lj, or
+        // lq == lj and the key's host is not after the query's
+        qbeg += (j - hj * a.S) + (hj > host ? 1 : 0);
+      } else if (a.causal) {
+        if (host < hj) continue;
+        qbeg = max(qbeg, j);
+      }
       for (int c = qbeg; c < qend; c += 32) {
         const int i = c + lane;
         float p = 0.f, ds = 0.f;

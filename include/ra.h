@@ -73,8 +73,19 @@ typedef enum { RA_F32 = 0, RA_BF16 = 1, RA_F16 = 2 } ra_dtype;
  *             hi + lo, taking its rounding from 2^-12 to about 2^-24
  *             relative at the cost of one more MMA per tile.  Needed when
  *             logits are large and values have outliers (e.g. |q| ~ 4 N(0,1)
- *             with +-50 entries in V); ignored for RA_F32. */
-enum { RA_CAUSAL = 1, RA_PRECISE = 2 };
+ *             with +-50 entries in V); ignored for RA_F32.
+ * RA_STRIPED  ring entry points with RA_CAUSAL: the rows of q, k, v, o, dO,
+ *             dq, dk, dv, lse are in striped order -- host i's local row l
+ *             (tensor row i*S + l) holds sequence position l*P + i -- so every
+ *             host has the same share of the causal triangle (load-balanced
+ *             ordering; "Striped Attention" is named beside Ring Attention on
+ *             "Ring Attention: Train 1M Tokens on 8GB GPUs in 2026", section
+ *             "How Does This Compare to Other Long-Context Methods?").  The
+ *             ring order is unchanged; every host visits every block, and in a
+ *             (query host i, key host j) pair local key row lk is visible to
+ *             local query row lq iff lk < lq, or lk == lq and j <= i.  Ignored
+ *             without RA_CAUSAL. */
+enum { RA_CAUSAL = 1, RA_PRECISE = 2, RA_STRIPED = 4 };
 
 typedef enum {
   RA_OK = 0,

@@ -13,5 +13,7 @@ from .attention import (  # noqa: F401
     merge_states,
     finalize_state,
     ring_fwd_blocked,
+    ring_fwd_blocked_striped,
+    striped_positions,
     ring_schedule,
 )

@@ -51,12 +51,13 @@ def _kv_head(h, hq, hkv):
     return h // (hq // hkv)
 
 
-def _visible(nq, nk, causal, q_off, kv_off):
-    """Boolean [nq, nk]: key j visible to query i (global positions)."""
+def _visible(nq, nk, causal, q_off, kv_off, q_pos=None, kv_pos=None):
+    """Boolean [nq, nk]: key j visible to query i.  Positions are q_off + i
+    and kv_off + j, or the explicit arrays q_pos, kv_pos when given."""
     if not causal:
         return np.ones((nq, nk), dtype=bool)
-    qpos = q_off + np.arange(nq)[:, None]
-    kpos = kv_off + np.arange(nk)[None, :]
+    qpos = (q_off + np.arange(nq) if q_pos is None else np.asarray(q_pos))[:, None]
+    kpos = (kv_off + np.arange(nk) if kv_pos is None else np.asarray(kv_pos))[None, :]
     return kpos <= qpos
 
 
@@ -241,15 +242,17 @@ def ring_schedule(P, causal):
     return sched
 
 
-def block_state(q, k, v, causal, scale, q_off, kv_off):
+def block_state(q, k, v, causal, scale, q_off, kv_off, q_pos=None, kv_pos=None):
     """Partial result of one (Q block, KV block) pair as the triple
     (m [B,Hq,Nq], l [B,Hq,Nq], o [B,Nq,Hq,d]):
     m_i = max_j s_ij, l_i = sum_j exp(s_ij - m_i), o_i = sum_j exp(s_ij - m_i) v_j.
-    A row with no visible key gives m = -inf, l = 0, o = 0."""
+    A row with no visible key gives m = -inf, l = 0, o = 0.  Sequence
+    positions default to q_off + row and kv_off + row (contiguous blocks);
+    q_pos / kv_pos give them explicitly (e.g. striped blocks)."""
     q, k, v = _f64(q), _f64(k), _f64(v)
     B, nq, hq, d = q.shape
     nk, hkv = k.shape[1], k.shape[2]
-    vis = _visible(nq, nk, causal, q_off, kv_off)
+    vis = _visible(nq, nk, causal, q_off, kv_off, q_pos, kv_pos)
     m = np.full((B, hq, nq), NEG_INF)
     l = np.zeros((B, hq, nq))
     o = np.zeros((B, nq, hq, d))
@@ -296,6 +299,42 @@ def finalize_state(state):
     inv = np.zeros_like(l)
     inv[ok] = 1.0 / l[ok]
     O = o * np.transpose(inv, (0, 2, 1))[..., None]
+    return O, LSE
+
+
+def striped_positions(N, P):
+    """Striped layout (load-balanced causal ordering, "Striped Attention" named
+    on "Ring Attention: Train 1M Tokens on 8GB GPUs in 2026", comparison
+    section): row r of a striped tensor, in host h = r // S at local row
+    l = r % S, holds sequence position l * P + h."""
+    if N % P:
+        raise ValueError("P must divide N")
+    S = N // P
+    r = np.arange(N)
+    return (r % S) * P + r // S
+
+
+def ring_fwd_blocked_striped(q, k, v, P, scale):
+    """Causal forward of the ring on a striped layout: q, k, v are given in
+    striped row order; host i holds rows [iS, (i+1)S) (sequence positions
+    l * P + i) and merges its queries' partial results against every KV chunk
+    in ring order (i - s) mod P.  Returns O, LSE in the same striped order."""
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    B, n, hq, d = q.shape
+    S = n // P
+    pos = striped_positions(n, P)
+    O = np.zeros((B, n, hq, d))
+    LSE = np.full((B, hq, n), NEG_INF)
+    for i, blocks in enumerate(ring_schedule(P, False)):
+        qi = q[:, i * S:(i + 1) * S]
+        acc = (np.full((B, hq, S), NEG_INF), np.zeros((B, hq, S)), np.zeros((B, S, hq, d)))
+        for j in blocks:
+            part = block_state(qi, k[:, j * S:(j + 1) * S], v[:, j * S:(j + 1) * S], True, scale, 0, 0,
+                               q_pos=pos[i * S:(i + 1) * S], kv_pos=pos[j * S:(j + 1) * S])
+            acc = merge_states(acc, part)
+        Oi, Li = finalize_state(acc)
+        O[:, i * S:(i + 1) * S] = Oi
+        LSE[:, :, i * S:(i + 1) * S] = Li
     return O, LSE
 
 

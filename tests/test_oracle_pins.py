@@ -308,3 +308,36 @@ def test_planted_missing_D_term_in_backward_is_caught():
     assert np.abs(dk_broken.sum(axis=0)).max() > 1e-6
     _, dk, *_ = A.attention_bwd(q, k, v, do, True, scale)
     assert np.abs(dk.sum(axis=1)).max() < 1e-12
+
+
+# --- striped (load-balanced) ordering -----------------------------------------
+
+def test_striped_positions_are_a_round_robin_permutation():
+    pos = oracle.striped_positions(12, 3)
+    assert sorted(pos) == list(range(12))
+    # host 0 holds 0, 3, 6, 9; host 1 holds 1, 4, 7, 10; host 2 holds 2, 5, 8, 11
+    assert list(pos) == [0, 3, 6, 9, 1, 4, 7, 10, 2, 5, 8, 11]
+
+
+@pytest.mark.parametrize("P", [1, 2, 3, 4, 6])
+def test_striped_ring_equals_plain_definition(P):
+    N = 12
+    q, k, v = rand(2, N, 4, 5, scale=2.0), rand(2, N, 2, 5), rand(2, N, 2, 5)
+    pos = oracle.striped_positions(N, P)
+    # striped layout: row r holds sequence position pos[r]
+    Os, Ls = oracle.ring_fwd_blocked_striped(q[:, pos], k[:, pos], v[:, pos], P, 0.6)
+    O, L = oracle.attention_fwd(q, k, v, True, 0.6)
+    np.testing.assert_allclose(Os, O[:, pos], atol=1e-12)
+    np.testing.assert_allclose(Ls, L[:, :, pos], atol=1e-12)
+
+
+def test_striped_blocks_share_the_causal_work_evenly():
+    # every (query host, key host) pair sees about half of its S x S pairs
+    N, P = 64, 4
+    S = N // P
+    pos = oracle.striped_positions(N, P)
+    vis = pos[None, :] <= pos[:, None]
+    counts = [[int(vis[i * S:(i + 1) * S, j * S:(j + 1) * S].sum()) for j in range(P)] for i in range(P)]
+    for i in range(P):
+        for j in range(P):
+            assert counts[i][j] == (S * (S + 1) // 2 if j <= i else S * (S - 1) // 2)
