@@ -19,7 +19,7 @@ __all__ = [
     "RAError", "RaShape", "lib", "shape_of",
     "ra_acc_init", "ra_block_fwd", "ra_block_fwd_workspace_bytes", "ra_merge", "ra_finalize",
     "ra_ring_fwd", "ra_ring_fwd_workspace_bytes", "ra_ring_bwd", "ra_ring_bwd_workspace_bytes",
-    "ra_ring_fwd_noalloc",
+    "ra_ring_fwd_noalloc", "ra_ring_fwd_varlen", "ra_ring_bwd_varlen",
     "ra_sync_status", "ra_last_error", "ra_launch_count", "ra_selftest_timeout",
     "ra_kernel_timing", "ra_kernel_timing_read",
     "ring_attention_fwd", "ring_attention_bwd", "RA_F32", "RA_BF16", "RA_F16",
@@ -67,6 +67,8 @@ def _load():
         "ra_ring_fwd": (i, [vp, vp, vp, i, sh, i, i, f, vp, i, vp, vp, sz, vp]),
         "ra_ring_fwd_workspace_bytes": (sz, [i, sh, i]),
         "ra_ring_fwd_noalloc": (i, [vp, vp, vp, i, sh, i, i, f, vp, i, vp, vp]),
+        "ra_ring_fwd_varlen": (i, [vp, vp, vp, i, sh, i, vp, i, f, vp, i, vp, vp, sz, vp]),
+        "ra_ring_bwd_varlen": (i, [vp, vp, vp, vp, i, vp, vp, i, sh, i, vp, i, f, vp, vp, vp, i, vp, sz, vp]),
         "ra_ring_bwd": (i, [vp, vp, vp, vp, i, vp, vp, i, sh, i, i, f, vp, vp, vp, i, vp, sz, vp]),
         "ra_ring_bwd_workspace_bytes": (sz, [i, i, sh, i]),
         "ra_sync_status": (i, [vp]),
@@ -216,6 +218,27 @@ def ra_ring_fwd_noalloc(q, k, v, P, causal, scale, o, lse, stream=None, precise=
                                    _ptr(lse), _stream(stream)))
 
 
+def ra_ring_fwd_varlen(q, k, v, P, host_len, causal, scale, o, lse, workspace=None, stream=None,
+                       precise=False):
+    """Ring forward where host i's first host_len[i] rows are valid (host_len:
+    int32 device tensor of P entries) and the rest is padding."""
+    shape = shape_of(q, k)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(lib.ra_ring_fwd_varlen(_ptr(q), _ptr(k), _ptr(v), _dt(q), shape, int(P), _ptr(host_len),
+                                  _flags(causal, precise), float(scale), _ptr(o), _dt(o), _ptr(lse),
+                                  _ptr(workspace), ws_bytes, _stream(stream)))
+
+
+def ra_ring_bwd_varlen(q, k, v, o, dO, lse, P, host_len, causal, scale, dq, dk, dv, workspace,
+                       stream=None, precise=False):
+    shape = shape_of(q, k)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(lib.ra_ring_bwd_varlen(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _dt(o), _ptr(dO), _ptr(lse),
+                                  _dt(q), shape, int(P), _ptr(host_len), _flags(causal, precise),
+                                  float(scale), _ptr(dq), _ptr(dk), _ptr(dv), _dt(dq), _ptr(workspace),
+                                  ws_bytes, _stream(stream)))
+
+
 def ra_ring_bwd_workspace_bytes(dtype, grad_dtype, shape, P):
     return int(lib.ra_ring_bwd_workspace_bytes(dtype, grad_dtype, shape, P))
 
@@ -239,7 +262,7 @@ def _workspace(nbytes, device):
 
 
 def ring_attention_fwd(q, k, v, P, causal=True, scale=None, o_dtype=torch.float32,
-                       stream=None, precise=False, striped=False):
+                       stream=None, precise=False, striped=False, host_len=None):
     """Allocate O [B,N,Hq,d] (o_dtype) and LSE [B,Hq,N] fp32 and run the ring forward."""
     if scale is None:
         scale = q.shape[-1] ** -0.5
@@ -247,12 +270,18 @@ def ring_attention_fwd(q, k, v, P, causal=True, scale=None, o_dtype=torch.float3
     o = torch.empty(B, N, Hq, d, dtype=o_dtype, device=q.device)
     lse = torch.empty(B, Hq, N, dtype=torch.float32, device=q.device)
     ws = _workspace(ra_ring_fwd_workspace_bytes(_dt(q), shape_of(q, k), P), q.device)
-    ra_ring_fwd(q, k, v, P, causal, scale, o, lse, ws, stream, precise, striped)
+    if host_len is not None:
+        if striped:
+            raise RAError(1, "striped layouts do not combine with per-host lengths")
+        ra_ring_fwd_varlen(q, k, v, P, host_len, causal, scale, o, lse, ws, stream, precise)
+    else:
+        ra_ring_fwd(q, k, v, P, causal, scale, o, lse, ws, stream, precise, striped)
     return o, lse
 
 
 def ring_attention_bwd(q, k, v, o, lse, dO, P, causal=True, scale=None,
-                       grad_dtype=torch.float32, stream=None, precise=False, striped=False):
+                       grad_dtype=torch.float32, stream=None, precise=False, striped=False,
+                       host_len=None):
     """Allocate dQ, dK, dV (grad_dtype) and workspace and run the ring backward."""
     if scale is None:
         scale = q.shape[-1] ** -0.5
@@ -261,5 +290,10 @@ def ring_attention_bwd(q, k, v, o, lse, dO, P, causal=True, scale=None,
     dv = torch.empty(v.shape, dtype=grad_dtype, device=q.device)
     ws = _workspace(ra_ring_bwd_workspace_bytes(_dt(q), _DTYPES[grad_dtype], shape_of(q, k), P),
                     q.device)
-    ra_ring_bwd(q, k, v, o, dO, lse, P, causal, scale, dq, dk, dv, ws, stream, precise, striped)
+    if host_len is not None:
+        if striped:
+            raise RAError(1, "striped layouts do not combine with per-host lengths")
+        ra_ring_bwd_varlen(q, k, v, o, dO, lse, P, host_len, causal, scale, dq, dk, dv, ws, stream, precise)
+    else:
+        ra_ring_bwd(q, k, v, o, dO, lse, P, causal, scale, dq, dk, dv, ws, stream, precise, striped)
     return dq, dk, dv

@@ -471,13 +471,15 @@ static int check_ring(const Shape& s, int P, int dtype) {
   return RA_OK;
 }
 
-int ra_ring_fwd(const void* q, const void* k, const void* v, ra_dtype dtype, ra_shape shape,
-                int P, int flags, float scale, void* o, ra_dtype o_dtype, float* lse,
-                void* workspace, size_t ws_bytes, void* stream) {
+static int ring_fwd_impl(const void* q, const void* k, const void* v, ra_dtype dtype, ra_shape shape,
+                         int P, int flags, float scale, void* o, ra_dtype o_dtype, float* lse,
+                         void* workspace, size_t ws_bytes, void* stream, const int* host_len) {
   const int causal = (flags & RA_CAUSAL) != 0, precise = (flags & RA_PRECISE) != 0;
   const int striped = causal && (flags & RA_STRIPED) != 0;
   if (flags & ~(RA_CAUSAL | RA_PRECISE | RA_STRIPED))
     return fail(RA_ERR_INVALID_ARG, "unknown flag bits 0x%x", flags);
+  if (host_len && striped)
+    return fail(RA_ERR_INVALID_ARG, "RA_STRIPED does not combine with per-host lengths");
   Shape s;
   int rc;
   if ((rc = check_shape(shape, &s))) return rc;
@@ -500,7 +502,7 @@ int ra_ring_fwd(const void* q, const void* k, const void* v, ra_dtype dtype, ra_
     a.B = s.B; a.Nq = s.Nq; a.Nkv = s.Nkv; a.Hq = s.Hq; a.Hkv = s.Hkv; a.d = s.d;
     a.q_bs = s.q_bs; a.kv_bs = s.kv_bs;
     a.scale = scale; a.causal = causal;
-    a.P = P; a.S = s.Nq / P; a.striped = striped;
+    a.P = P; a.S = s.Nq / P; a.striped = striped; a.host_len = host_len;
     a.o_out = o; a.o_dtype = o_dtype; a.o_bs = s.q_bs; a.lse = lse;
     TimedLaunch tl(RA_KERNEL_FWD_F32, cs);
     cudaError_t e = launch_simt_fwd(a, cs);
@@ -531,6 +533,11 @@ int ra_ring_fwd(const void* q, const void* k, const void* v, ra_dtype dtype, ra_
   a.scale_log2 = scale * 1.4426950408889634f;
   a.causal = causal;
   a.ring_P = P; a.ring_S = s.Nq / P; a.mode = 0; a.precise = precise; a.striped = striped;
+  a.host_len = host_len;
+  if (host_len) {  // padded rows: O = 0, LSE = -inf (the kernel skips them)
+    cudaError_t fe = launch_fill_padding(o, o_dtype, s.q_bs, s.B, s.Nq, s.Hq, s.d, P, host_len, lse, cs);
+    if (fe != cudaSuccess) return cuda_fail(fe, "padding fill launch");
+  }
   a.o_out = o; a.o_dtype = o_dtype; a.o_bs = s.q_bs; a.lse = lse;
   a.status = st;
   a.wait_limit_ns = wait_limit_ns();
@@ -573,14 +580,16 @@ size_t ra_ring_bwd_workspace_bytes(ra_dtype dtype, ra_dtype grad_dtype, ra_shape
   return bwd_layout(dtype, shape).total;
 }
 
-int ra_ring_bwd(const void* q, const void* k, const void* v, const void* o, ra_dtype o_dtype,
-                const void* dO, const float* lse, ra_dtype dtype, ra_shape shape, int P,
-                int flags, float scale, void* dq, void* dk, void* dv, ra_dtype grad_dtype,
-                void* workspace, size_t ws_bytes, void* stream) {
+static int ring_bwd_impl(const void* q, const void* k, const void* v, const void* o, ra_dtype o_dtype,
+                         const void* dO, const float* lse, ra_dtype dtype, ra_shape shape, int P,
+                         int flags, float scale, void* dq, void* dk, void* dv, ra_dtype grad_dtype,
+                         void* workspace, size_t ws_bytes, void* stream, const int* host_len) {
   const int causal = (flags & RA_CAUSAL) != 0, precise = (flags & RA_PRECISE) != 0;
   const int striped = causal && (flags & RA_STRIPED) != 0;
   if (flags & ~(RA_CAUSAL | RA_PRECISE | RA_STRIPED))
     return fail(RA_ERR_INVALID_ARG, "unknown flag bits 0x%x", flags);
+  if (host_len && striped)
+    return fail(RA_ERR_INVALID_ARG, "RA_STRIPED does not combine with per-host lengths");
   Shape s;
   int rc;
   if ((rc = check_shape(shape, &s))) return rc;
@@ -617,7 +626,7 @@ int ra_ring_bwd(const void* q, const void* k, const void* v, const void* o, ra_d
     a.B = s.B; a.N = s.Nq; a.Hq = s.Hq; a.Hkv = s.Hkv; a.d = s.d;
     a.q_bs = s.q_bs; a.kv_bs = s.kv_bs;
     a.scale = scale; a.causal = causal;
-    a.P = P; a.S = s.Nq / P; a.striped = striped;
+    a.P = P; a.S = s.Nq / P; a.striped = striped; a.host_len = host_len;
     a.dq = dq; a.dk = dk; a.dv = dv; a.grad_dtype = grad_dtype;
     {
       TimedLaunch tl(RA_KERNEL_BWD_F32, cs);
@@ -658,6 +667,13 @@ int ra_ring_bwd(const void* q, const void* k, const void* v, const void* o, ra_d
   a.scale_log2 = scale * 1.4426950408889634f;
   a.causal = causal;
   a.ring_P = P; a.ring_S = s.Nq / P; a.precise = precise; a.striped = striped;
+  a.host_len = host_len;
+  if (host_len) {  // padded key rows: dK = dV = 0 (the kernel skips wholly padded key tiles)
+    cudaError_t fe = launch_fill_padding(dk, grad_dtype, s.kv_bs, s.B, s.Nkv, s.Hkv, s.d, P, host_len, nullptr, cs);
+    if (fe == cudaSuccess)
+      fe = launch_fill_padding(dv, grad_dtype, s.kv_bs, s.B, s.Nkv, s.Hkv, s.d, P, host_len, nullptr, cs);
+    if (fe != cudaSuccess) return cuda_fail(fe, "padding fill launch");
+  }
   a.lse = lse2; a.Dvec = Dv; a.dq_acc = dq_acc;
   a.dk = dk; a.dv = dv; a.grad_dtype = grad_dtype; a.kv_bs = s.kv_bs;
   a.status = st;
@@ -670,6 +686,40 @@ int ra_ring_bwd(const void* q, const void* k, const void* v, const void* o, ra_d
   if (e != cudaSuccess) return cuda_fail(e, "tensor-core ring backward launch");
   e = launch_f32_to(dq_acc, dq, grad_dtype, s.q_bs, s.B, qel, scale, cs);
   return e == cudaSuccess ? RA_OK : cuda_fail(e, "dq conversion launch");
+}
+
+int ra_ring_fwd(const void* q, const void* k, const void* v, ra_dtype dtype, ra_shape shape,
+                int P, int flags, float scale, void* o, ra_dtype o_dtype, float* lse,
+                void* workspace, size_t ws_bytes, void* stream) {
+  return ring_fwd_impl(q, k, v, dtype, shape, P, flags, scale, o, o_dtype, lse, workspace, ws_bytes,
+                       stream, nullptr);
+}
+
+int ra_ring_bwd(const void* q, const void* k, const void* v, const void* o, ra_dtype o_dtype,
+                const void* dO, const float* lse, ra_dtype dtype, ra_shape shape, int P,
+                int flags, float scale, void* dq, void* dk, void* dv, ra_dtype grad_dtype,
+                void* workspace, size_t ws_bytes, void* stream) {
+  return ring_bwd_impl(q, k, v, o, o_dtype, dO, lse, dtype, shape, P, flags, scale, dq, dk, dv,
+                       grad_dtype, workspace, ws_bytes, stream, nullptr);
+}
+
+int ra_ring_fwd_varlen(const void* q, const void* k, const void* v, ra_dtype dtype, ra_shape shape,
+                       int P, const int* host_len, int flags, float scale, void* o, ra_dtype o_dtype,
+                       float* lse, void* workspace, size_t ws_bytes, void* stream) {
+  if (!host_len || (reinterpret_cast<uintptr_t>(host_len) & 3u))
+    return fail(RA_ERR_INVALID_ARG, "host_len must be a non-NULL, 4-byte aligned device array");
+  return ring_fwd_impl(q, k, v, dtype, shape, P, flags, scale, o, o_dtype, lse, workspace, ws_bytes,
+                       stream, host_len);
+}
+
+int ra_ring_bwd_varlen(const void* q, const void* k, const void* v, const void* o, ra_dtype o_dtype,
+                       const void* dO, const float* lse, ra_dtype dtype, ra_shape shape, int P,
+                       const int* host_len, int flags, float scale, void* dq, void* dk, void* dv,
+                       ra_dtype grad_dtype, void* workspace, size_t ws_bytes, void* stream) {
+  if (!host_len || (reinterpret_cast<uintptr_t>(host_len) & 3u))
+    return fail(RA_ERR_INVALID_ARG, "host_len must be a non-NULL, 4-byte aligned device array");
+  return ring_bwd_impl(q, k, v, o, o_dtype, dO, lse, dtype, shape, P, flags, scale, dq, dk, dv,
+                       grad_dtype, workspace, ws_bytes, stream, host_len);
 }
 
 }  // extern "C"

@@ -87,7 +87,9 @@ struct BwdUnit {
 // accumulator rows they sweep stay in L2 (one head of them is ~128 MB at
 // N = 131072).  Within a head the earliest key tiles come first: under a
 // causal mask they have the most work.
-template <bool STRIPED>
+__device__ __forceinline__ int host_len_at(const int* hl, int j, int S);
+
+template <bool STRIPED, bool VARLEN>
 __device__ __forceinline__ BwdUnit bwd_unit(const TcBwdArgs& a, int u) {
   BwdUnit r;
   const int nT = a.N / 128;
@@ -110,6 +112,13 @@ __device__ __forceinline__ BwdUnit bwd_unit(const TcBwdArgs& a, int u) {
   }
   r.count = a.causal ? nT - r.jt : nT;
   r.n_iter = r.count * (a.Hq / a.Hkv);
+  if (VARLEN) {
+    // key tiles wholly in their host's padding do no work (their dK, dV rows
+    // were zero-filled beforehand)
+    const int T = a.ring_S / 128;
+    const int j = r.jt / T;
+    if ((r.jt - j * T) * 128 >= host_len_at(a.host_len, j, a.ring_S)) r.n_iter = 0;
+  }
   return r;
 }
 
@@ -134,6 +143,20 @@ __device__ __forceinline__ void bwd_iter(const TcBwdArgs& a, const BwdUnit& u, i
     const int hj = u.jt / T;
     *qt = (hj * T + k) % nT;
   }
+}
+
+// Variable host lengths: valid rows of host j (clamped to [0, S]); a query
+// tile wholly in its host's padding is skipped by every role.
+__device__ __forceinline__ int host_len_at(const int* hl, int j, int S) {
+  const int v = __ldg(hl + j);
+  return v < 0 ? 0 : (v > S ? S : v);
+}
+template <bool VARLEN>
+__device__ __forceinline__ bool q_tile_valid(const TcBwdArgs& a, int qt) {
+  if (!VARLEN) return true;
+  const int T = a.ring_S / 128;
+  const int i = qt / T;
+  return (qt - i * T) * 128 < host_len_at(a.host_len, i, a.ring_S);
 }
 
 __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes,
@@ -168,9 +191,14 @@ __device__ __forceinline__ uint32_t dq_box(int s, int cc) {
   return L::kDO0 + s * L::kTile + cc * 16384;
 }
 
-template <int D, bool PRECISE, bool STRIPED>
+// Ring layouts, one kernel build each: contiguous hosts, striped rows, and
+// contiguous hosts with variable valid lengths.
+enum { kLayoutContiguous = 0, kLayoutStriped = 1, kLayoutVarlen = 2 };
+
+template <int D, bool PRECISE, int LAYOUT>
 __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_constant__ TcBwdArgs a) {
   using L = BwdSmem<D>;
+  constexpr bool STRIPED = LAYOUT == kLayoutStriped, VARLEN = LAYOUT == kLayoutVarlen;
   extern __shared__ __align__(1024) uint8_t smem[];
   const uint32_t sbase = smem_u32(smem);
   if (sbase & 1023u) {  // the swizzled tiles need 1024-byte alignment
@@ -244,8 +272,11 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
       int q_issued[2] = {0, 0}, do_issued[2] = {0, 0};
       int k = 0;
       bool ok = true;
+      // k counts the units this CTA has worked on; a key tile wholly in
+      // padding is no unit
       for (int u = blockIdx.x; u < a.num_units && ok; u += gridDim.x, ++k) {
-        const BwdUnit bu = bwd_unit<STRIPED>(a, u);
+        const BwdUnit bu = bwd_unit<STRIPED, VARLEN>(a, u);
+        if (VARLEN && bu.n_iter == 0) { --k; continue; }
         if (!mbar_wait(BAR_KV_EMPTY, (k & 1) ^ 1, abort_flag, a.status, lim)) { ok = false; break; }
         mbar_arrive_expect_tx(BAR_KV_FULL, 2 * L::kTile);
 #pragma unroll
@@ -256,6 +287,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
         for (int it = 0; it < bu.n_iter; ++it) {
           int h, qt;
           bwd_iter<STRIPED>(a, bu, it, &h, &qt);
+          if (VARLEN && !q_tile_valid<VARLEN>(a, qt)) continue;
           const int s = qd_cnt & 1;
           const uint32_t par = ((qd_cnt >> 1) & 1) ^ 1;
           if (!mbar_wait(bar_q_empty(s), par, abort_flag, a.status, lim)) { ok = false; break; }
@@ -320,8 +352,18 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
         tc_fence_after();
         return ok;
       };
+      // next query tile at or after iteration it that is not wholly padding
+      auto next_valid = [&](const BwdUnit& bu, int it) {
+        for (; it < bu.n_iter; ++it) {
+          int h, qt;
+          bwd_iter<STRIPED>(a, bu, it, &h, &qt);
+          if (q_tile_valid<VARLEN>(a, qt)) break;
+        }
+        return it;
+      };
       for (int u = blockIdx.x; u < a.num_units && ok; u += gridDim.x, ++k) {
-        const BwdUnit bu = bwd_unit<STRIPED>(a, u);
+        const BwdUnit bu = bwd_unit<STRIPED, VARLEN>(a, u);
+        if (VARLEN && bu.n_iter == 0) { --k; continue; }
         if (!wait(BAR_KV_FULL, k & 1)) break;
         // prologue: S(0), dP(0)
         uint32_t s = qd_cnt & 1;
@@ -332,18 +374,20 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
         if (!wait(bar_do_full(s), (qd_cnt >> 1) & 1)) break;
         mma_nt(T_DP, dV_k, dO_k0 + s * kStageStep);
         mma_commit(BAR_DP_FULL);
-        for (int it = 0; it < bu.n_iter; ++it) {
+        const int it0 = VARLEN ? next_valid(bu, 0) : 0;
+        for (int it = it0, nx; it < bu.n_iter; it = nx) {
+          nx = VARLEN ? next_valid(bu, it + 1) : it + 1;
           const uint64_t dQ_mn = dQ_mn0 + s * kStageStep, dO_mn = dO_mn0 + s * kStageStep;
           if (!wait(BAR_DS_FULL, ds_cnt & 1)) break;
           ++ds_cnt;
-          if (it == 0 && k > 0 && !wait(BAR_DKV_FREE, (k - 1) & 1)) break;
+          if (it == it0 && k > 0 && !wait(BAR_DKV_FREE, (k - 1) & 1)) break;
           // dV += P^T dO_i   (P^T in TMEM: queries 0-63 at columns 0-31, 64-127 at 64-95)
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk) {
             const uint32_t pa = T_S + (kk < 4 ? kk * 8 : 64 + (kk - 4) * 8);
-            mma_ts(T_DV, pa, desc_off(dO_mn, kk * 2048), id_acc, (it > 0 || kk > 0) ? 1u : 0u);
+            mma_ts(T_DV, pa, desc_off(dO_mn, kk * 2048), id_acc, (it > it0 || kk > 0) ? 1u : 0u);
           }
-          const bool has_next = it + 1 < bu.n_iter;
+          const bool has_next = nx < bu.n_iter;
           const uint32_t s2 = (qd_cnt + 1) & 1, par2 = ((qd_cnt + 1) >> 1) & 1;
           if (has_next) {
             if (!wait(bar_q_full(s2), par2)) break;
@@ -354,7 +398,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk) {
             const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-            mma_ss(T_DK, desc_off(dS_k, off), desc_off(dQ_mn, kk * 2048), id_acc, (it > 0 || kk > 0) ? 1u : 0u);
+            mma_ss(T_DK, desc_off(dS_k, off), desc_off(dQ_mn, kk * 2048), id_acc, (it > it0 || kk > 0) ? 1u : 0u);
           }
           if (PRECISE) {  // + dS_lo^T Q_i, dS_lo^T in TMEM (queries 0-63 at dP columns 0-31, 64-127 at 64-95)
 #pragma unroll
@@ -401,10 +445,11 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
     uint32_t gi = 0;  // iterations done by this CTA (all units)
     bool ok = true;
     for (int u = blockIdx.x; u < a.num_units && ok; u += gridDim.x) {
-      const BwdUnit bu = bwd_unit<STRIPED>(a, u);
+      const BwdUnit bu = bwd_unit<STRIPED, VARLEN>(a, u);
       for (int it = 0; it < bu.n_iter; ++it, ++gi) {
         int h, qt;
         bwd_iter<STRIPED>(a, bu, it, &h, &qt);
+        if (VARLEN && !q_tile_valid<VARLEN>(a, qt)) { --gi; continue; }
         const int s = gi & 1;
         const float* lse2 = reinterpret_cast<const float*>(smem + L::kVec0 + s * 1024) + half * 64;
         const float* dvec = lse2 + 128;
@@ -420,6 +465,14 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
         // c visible to key row r iff c >= r); for a striped layout the same
         // local tile of any host pair, strict (c > r) when the key's host
         // comes after the query's
+        // padding: query columns from qvalid on, key rows from kvalid on
+        int qvalid = 128, kvalid = 128;
+        if (VARLEN) {
+          const int T = a.ring_S / 128;
+          qvalid = host_len_at(a.host_len, qt / T, a.ring_S) - (qt % T) * 128;
+          kvalid = host_len_at(a.host_len, bu.jt / T, a.ring_S) - (bu.jt % T) * 128;
+        }
+        const bool pad = qvalid < 128 || kvalid < 128;
         bool diag;
         int strict = 0;
         if (STRIPED) {
@@ -438,6 +491,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
           for (int u4 = 0; u4 < 4; ++u4) {
             float p = ex2_approx(fmaf(__uint_as_float(pr[c + u4]), sl2, -lv[u4]));
             if (diag && half * 64 + c + u4 < r + strict) p = 0.f;
+            if (VARLEN && pad && (half * 64 + c + u4 >= qvalid || r >= kvalid)) p = 0.f;
             pr[c + u4] = __float_as_uint(p);
           }
         }
@@ -497,10 +551,12 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
     int k = 0;
     bool ok = true;
     for (int u = blockIdx.x; u < a.num_units && ok; u += gridDim.x, ++k) {
-      const BwdUnit bu = bwd_unit<STRIPED>(a, u);
+      const BwdUnit bu = bwd_unit<STRIPED, VARLEN>(a, u);
+      if (VARLEN && bu.n_iter == 0) { --k; continue; }
       for (int it = 0; it < bu.n_iter; ++it) {
         int h, qt;
         bwd_iter<STRIPED>(a, bu, it, &h, &qt);
+        if (VARLEN && !q_tile_valid<VARLEN>(a, qt)) continue;
         if (!mbar_wait(BAR_DQ_FULL, dq_cnt & 1, abort_flag, a.status, lim)) { ok = false; break; }
         ++dq_cnt;
         tc_fence_after();
@@ -629,18 +685,24 @@ cudaError_t launch_tc_bwd(TcBwdArgs& a, int num_sms, cudaStream_t st) {
   };
   if (a.d == 128) {
     if (a.striped)
-      e = a.precise ? run(tc_bwd_kernel<128, true, true>, BwdSmem<128>::kBytes)
-                    : run(tc_bwd_kernel<128, false, true>, BwdSmem<128>::kBytes);
+      e = a.precise ? run(tc_bwd_kernel<128, true, kLayoutStriped>, BwdSmem<128>::kBytes)
+                    : run(tc_bwd_kernel<128, false, kLayoutStriped>, BwdSmem<128>::kBytes);
+    else if (a.host_len)
+      e = a.precise ? run(tc_bwd_kernel<128, true, kLayoutVarlen>, BwdSmem<128>::kBytes)
+                    : run(tc_bwd_kernel<128, false, kLayoutVarlen>, BwdSmem<128>::kBytes);
     else
-      e = a.precise ? run(tc_bwd_kernel<128, true, false>, BwdSmem<128>::kBytes)
-                    : run(tc_bwd_kernel<128, false, false>, BwdSmem<128>::kBytes);
+      e = a.precise ? run(tc_bwd_kernel<128, true, kLayoutContiguous>, BwdSmem<128>::kBytes)
+                    : run(tc_bwd_kernel<128, false, kLayoutContiguous>, BwdSmem<128>::kBytes);
   } else if (a.d == 64) {
     if (a.striped)
-      e = a.precise ? run(tc_bwd_kernel<64, true, true>, BwdSmem<64>::kBytes)
-                    : run(tc_bwd_kernel<64, false, true>, BwdSmem<64>::kBytes);
+      e = a.precise ? run(tc_bwd_kernel<64, true, kLayoutStriped>, BwdSmem<64>::kBytes)
+                    : run(tc_bwd_kernel<64, false, kLayoutStriped>, BwdSmem<64>::kBytes);
+    else if (a.host_len)
+      e = a.precise ? run(tc_bwd_kernel<64, true, kLayoutVarlen>, BwdSmem<64>::kBytes)
+                    : run(tc_bwd_kernel<64, false, kLayoutVarlen>, BwdSmem<64>::kBytes);
     else
-      e = a.precise ? run(tc_bwd_kernel<64, true, false>, BwdSmem<64>::kBytes)
-                    : run(tc_bwd_kernel<64, false, false>, BwdSmem<64>::kBytes);
+      e = a.precise ? run(tc_bwd_kernel<64, true, kLayoutContiguous>, BwdSmem<64>::kBytes)
+                    : run(tc_bwd_kernel<64, false, kLayoutContiguous>, BwdSmem<64>::kBytes);
   } else {
     return cudaErrorInvalidValue;
   }

@@ -84,6 +84,11 @@ struct UnitInfo {
   int striped, host, P, T, L, tq[2];
 };
 
+__device__ __forceinline__ int host_len_at(const int* hl, int j, int S) {
+  const int v = __ldg(hl + j);
+  return v < 0 ? 0 : (v > S ? S : v);
+}
+
 // Key/value tile of iteration it: global tile kt, and for striped layouts the
 // local tile tk and the block j it belongs to.
 __device__ __forceinline__ int kt_at(const UnitInfo& u, int it, int* tk = nullptr, int* blk = nullptr) {
@@ -99,6 +104,21 @@ __device__ __forceinline__ int kt_at(const UnitInfo& u, int it, int* tk = nullpt
   int kt = u.kt0 - it;
   if (u.wrap && kt < 0) kt += u.nkt;
   return kt;
+}
+
+// With variable host lengths a key/value tile wholly in a host's padding is
+// skipped by every role.
+__device__ __forceinline__ bool iter_valid(const UnitInfo& u, int it, const int* host_len, int ring_S) {
+  int kt = u.kt0 - it;  // contiguous ring tiles
+  if (u.wrap && kt < 0) kt += u.nkt;
+  const int T = ring_S / 128;
+  const int j = kt / T, tk = kt - j * T;
+  return tk * 128 < host_len_at(host_len, j, ring_S);
+}
+__device__ __forceinline__ int next_valid(const UnitInfo& u, int it, const int* host_len, int ring_S) {
+  ++it;
+  while (it < u.n_iter && !iter_valid(u, it, host_len, ring_S)) ++it;
+  return it;
 }
 
 // Does query tile x (0 = A, 1 = B) take part in iteration it?
@@ -129,6 +149,9 @@ __device__ __forceinline__ int last_visible_tile(const TcFwdArgs& a, long long q
 // of one (batch, head) together, which keeps them in L2), and within a head
 // from the last query tiles to the first: under a causal mask the last ones
 // see the most keys.
+// VARLEN selects the kernel built for variable host lengths; the other
+// builds see no length array and compile its checks away.
+template <bool VARLEN>
 __device__ __forceinline__ UnitInfo unit_info(const TcFwdArgs& a, int u) {
   UnitInfo r;
   int per_head;
@@ -195,6 +218,23 @@ __device__ __forceinline__ UnitInfo unit_info(const TcFwdArgs& a, int u) {
       r.start[0] = 0;
       r.start[1] = 0;
     }
+    if (VARLEN && a.host_len) {
+      // query tiles wholly in the host's padding do no work (their rows were
+      // filled with O = 0, LSE = -inf beforehand)
+      const int qlen = host_len_at(a.host_len, host, a.ring_S);
+      const int la = lp * 256;
+      if (la >= qlen) r.n_iter = 0;
+      if (la + 128 >= qlen && r.has_b) {
+        r.has_b = 0;
+        r.start[1] = r.n_iter;
+        if (a.causal) {  // tile A leads
+          r.kt0 = ta;
+          r.n_iter = ta + 1;
+          r.start[0] = 0;
+          r.start[1] = r.n_iter;
+        }
+      }
+    }
   } else {
     const int nqt = (a.Nq + 127) / 128;
     const int total = (nqt + 1) / 2;
@@ -218,7 +258,7 @@ __device__ __forceinline__ UnitInfo unit_info(const TcFwdArgs& a, int u) {
   return r;
 }
 
-template <int D, bool PRECISE>
+template <int D, bool PRECISE, bool VARLEN>
 __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_constant__ TcFwdArgs a) {
   using L = FwdSmem<D>;
   extern __shared__ uint8_t smem_raw[];
@@ -284,7 +324,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
       for (int s = 0; s < kStages; ++s) issued[s] = 0, last_phase[s] = 0;
       int q_issued = 0;
       for (int u = blockIdx.x; u < a.num_units && ok; u += gridDim.x) {
-        const UnitInfo ui = unit_info(a, u);
+        const UnitInfo ui = unit_info<VARLEN>(a, u);
         if (ui.n_iter == 0) continue;  // no key of this block is visible to the unit
         if (!mbar_wait(BAR_Q_EMPTY, (k & 1) ^ 1, abort_flag, a.status, lim)) { ok = false; break; }
         ++k;
@@ -300,8 +340,9 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
                         ui.qa_row0 + 128, ui.b, pol_q);
         }
         for (int it = 0; it < ui.n_iter && ok; ++it) {
+          if (VARLEN && !iter_valid(ui, it, a.host_len, a.ring_S)) continue;
           int tk = 0, blk = 0;
-        const int kt = kt_at(ui, it, &tk, &blk);
+          const int kt = kt_at(ui, it, &tk, &blk);
 #pragma unroll
           for (int kv = 0; kv < 2; ++kv) {  // K then V
             const int s = L_cnt % kStages;
@@ -364,25 +405,27 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
         }
       };
       for (int u = blockIdx.x; u < a.num_units && ok; u += gridDim.x) {
-        const UnitInfo ui = unit_info(a, u);
+        const UnitInfo ui = unit_info<VARLEN>(a, u);
         if (ui.n_iter == 0) continue;
         if (!mbar_wait(BAR_Q_FULL, k & 1, abort_flag, a.status, lim)) { ok = false; break; }
         ++k;
         tc_fence_after();
-        // prologue: S(0)
+        // prologue: S of the first valid iteration
+        const int it0 = !VARLEN || iter_valid(ui, 0, a.host_len, a.ring_S) ? 0 : next_valid(ui, 0, a.host_len, a.ring_S);
         uint32_t sk = L_cnt % kStages;
         if (!mbar_wait(bar_kv_full(sk), (L_cnt / kStages) & 1, abort_flag, a.status, lim)) { ok = false; break; }
         tc_fence_after();
         for (int x = 0; x < 2; ++x)
-          if (active(ui, x, 0)) issue_s(x, sk);
+          if (active(ui, x, it0)) issue_s(x, sk);
         mma_commit(bar_kv_empty(sk));
         ++L_cnt;
         bool first_pv[2] = {a.mode == 0, a.mode == 0};
-        for (int it = 0; it < ui.n_iter; ++it) {
+        for (int it = it0, nx; it < ui.n_iter; it = nx) {
+          nx = VARLEN ? next_valid(ui, it, a.host_len, a.ring_S) : it + 1;
           const uint32_t sv = L_cnt % kStages;
           if (!mbar_wait(bar_kv_full(sv), (L_cnt / kStages) & 1, abort_flag, a.status, lim)) { ok = false; break; }
           ++L_cnt;
-          const bool has_next = it + 1 < ui.n_iter;
+          const bool has_next = nx < ui.n_iter;
           uint32_t sk2 = 0;
           if (has_next) {
             sk2 = L_cnt % kStages;
@@ -399,7 +442,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
               first_pv[x] = false;
               if (!has_next) mma_commit(bar_o_full(x));
             }
-            if (has_next && active(ui, x, it + 1)) issue_s(x, sk2);
+            if (has_next && active(ui, x, nx)) issue_s(x, sk2);
           }
           if (!ok) break;
           mma_commit(bar_kv_empty(sv));
@@ -424,10 +467,11 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
     uint32_t s_cnt = 0, o_cnt = 0;
     bool ok = true;
     for (int u = blockIdx.x; u < a.num_units && ok; u += gridDim.x) {
-      const UnitInfo ui = unit_info(a, u);
-      if (!ever_active(ui, x)) continue;  // this tile sees no key in this unit
+      const UnitInfo ui = unit_info<VARLEN>(a, u);
+      if ((VARLEN && ui.n_iter == 0) || !ever_active(ui, x)) continue;  // this tile sees no key in this unit
       const int row = ui.qa_row0 + x * 128 + r;  // tensor row
-      const bool row_ok = row < a.Nq;
+      // with variable host lengths, rows past their host's valid length are padding
+      const bool row_ok = row < a.Nq && (!VARLEN || row % a.ring_S < host_len_at(a.host_len, row / a.ring_S, a.ring_S));
       const long long qpos = ui.qpos0[x] + r;
       float m_run = -INFINITY, l_run = 0.f;
       const long long sidx = ((long long)ui.b * a.Hq + ui.h) * a.Nq + row;
@@ -456,7 +500,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
       }
       bool o_valid = (a.mode == 1);  // O_X holds a state that must be rescaled
       for (int it = ui.striped ? 0 : ui.start[x]; it < ui.n_iter; ++it) {
-        if (!active(ui, x, it)) continue;
+        if (!active(ui, x, it) || (VARLEN && !iter_valid(ui, it, a.host_len, a.ring_S))) continue;
         if (!mbar_wait(bar_s_full(x), s_cnt & 1, abort_flag, a.status, lim)) { ok = false; break; }
         ++s_cnt;
         tc_fence_after();
@@ -479,8 +523,15 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
           need_mask = (a.causal && kvpos0 + 127 > ui.qpos0[x]) || (kt * 128 + 128 > a.Nkv);
           lim_c = a.causal ? qpos - kvpos0 : 127;
         }
+        int kv_len = 128;
+        if (VARLEN) {  // keys past the key host's valid length
+          const int T = a.ring_S / 128;
+          const int j = kt / T;
+          kv_len = host_len_at(a.host_len, j, a.ring_S) - (kt - j * T) * 128;
+          if (kv_len < 128) need_mask = true;
+        }
         if (need_mask) {
-          const int nvalid = a.Nkv - kt * 128;
+          const int nvalid = VARLEN ? min(a.Nkv - kt * 128, kv_len) : a.Nkv - kt * 128;
 #pragma unroll
           for (int c = 0; c < 128; ++c)
             if (c > lim_c || c >= nvalid) sr[c] = __float_as_uint(-INFINITY);
@@ -613,11 +664,15 @@ cudaError_t launch_tc_fwd(TcFwdArgs& a, int num_sms, cudaStream_t st) {
     return cudaSuccess;
   };
   if (a.d == 128)
-    e = a.precise ? run(tc_fwd_kernel<128, true>, FwdSmem<128>::kAlloc)
-                  : run(tc_fwd_kernel<128, false>, FwdSmem<128>::kAlloc);
+    e = a.host_len ? (a.precise ? run(tc_fwd_kernel<128, true, true>, FwdSmem<128>::kAlloc)
+                                : run(tc_fwd_kernel<128, false, true>, FwdSmem<128>::kAlloc))
+                   : (a.precise ? run(tc_fwd_kernel<128, true, false>, FwdSmem<128>::kAlloc)
+                                : run(tc_fwd_kernel<128, false, false>, FwdSmem<128>::kAlloc));
   else if (a.d == 64)
-    e = a.precise ? run(tc_fwd_kernel<64, true>, FwdSmem<64>::kAlloc)
-                  : run(tc_fwd_kernel<64, false>, FwdSmem<64>::kAlloc);
+    e = a.host_len ? (a.precise ? run(tc_fwd_kernel<64, true, true>, FwdSmem<64>::kAlloc)
+                               : run(tc_fwd_kernel<64, false, true>, FwdSmem<64>::kAlloc))
+                   : (a.precise ? run(tc_fwd_kernel<64, true, false>, FwdSmem<64>::kAlloc)
+                                : run(tc_fwd_kernel<64, false, false>, FwdSmem<64>::kAlloc));
   else
     return cudaErrorInvalidValue;
   if (e != cudaSuccess) return e;

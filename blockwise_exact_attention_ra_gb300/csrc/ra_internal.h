@@ -32,6 +32,7 @@ struct SimtFwdArgs {
   long long q_off, kv_off;  // block mode: global positions of row 0
   int P, S;                 // ring mode: P hosts of S rows; P == 0 -> block mode
   int striped;              // ring mode, causal: rows in striped order (position l*P + host)
+  const int* host_len;      // ring mode, optional: valid rows per host (device, P entries)
   float* o_acc;             // block mode state (read + written)
   float* m_acc;
   float* l_acc;
@@ -54,6 +55,7 @@ struct SimtBwdArgs {
   int causal;
   int P, S;
   int striped;
+  const int* host_len;
   void* dq;
   void* dk;
   void* dv;
@@ -87,6 +89,11 @@ cudaError_t launch_bwd_dot(const void* dO, int do_dtype, const void* o, int o_dt
 // out (dtype, batch stride out_bs) <- mul * src (packed fp32)
 cudaError_t launch_f32_to(const float* src, void* out, int out_dtype, long long out_bs,
                           int B, long long elems_per_batch, float mul, cudaStream_t st);
+// Padded rows of a [B, N, H, d] tensor (row l of host i with l >= host_len[i],
+// S = N / P rows per host) are set to zero, and lse[b, h, row] to -inf when
+// lse is given.
+cudaError_t launch_fill_padding(void* t, int dtype, long long bs, int B, int N, int H, int d,
+                                int P, const int* host_len, float* lse, cudaStream_t st);
 cudaError_t launch_selftest_timeout(unsigned int timeout_us, int* status,
                                     cudaStream_t st);
 
@@ -105,6 +112,7 @@ struct TcFwdArgs {
   long long q_off, kv_off;
   int ring_P, ring_S;  // ring mode when ring_P > 0 (Nq == Nkv == P*S, S % 128 == 0)
   int striped;         // ring mode, causal: rows are in striped order (position l*P + host)
+  const int* host_len; // ring mode, optional: valid rows per host (device, P entries)
   // outputs
   int mode;         // 0: ring (finalise), 1: block (read/write state)
   float* o_acc;     // block mode: [B, Nq, Hq, d] fp32
@@ -133,6 +141,7 @@ struct TcBwdArgs {
   int precise;  // two-term fp16 dS in the dK product
   int ring_P, ring_S;
   int striped;  // causal, rows in striped order (position l*P + host)
+  const int* host_len;  // optional: valid rows per host (device, P entries)
   const float* lse;   // [B, Hq, N], multiplied by log2(e)
   const float* Dvec;  // [B, Hq, N]
   float* dq_acc;      // packed fp32 [B, N, Hq, d], pre-zeroed, reduce-added

@@ -34,6 +34,11 @@ __device__ __forceinline__ float load_dtype(const void* base, int dtype, long lo
   return __half2float(static_cast<const __half*>(base)[idx]);
 }
 
+__device__ __forceinline__ int clamp_len(const int* hl, int j, int S) {
+  const int v = __ldg(hl + j);
+  return v < 0 ? 0 : (v > S ? S : v);
+}
+
 // Keys [kbeg, kend) of one block against the warp's query row.  q_s holds the
 // query row (d floats); lane owns output columns lane + 32*t.
 template <int DPL>
@@ -107,6 +112,7 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32)
 #pragma unroll
     for (int t = 0; t < DPL; ++t) o[t] = 0.f;
     const int hi = i / a.S;
+    const bool padded = a.host_len && (i - hi * a.S) >= clamp_len(a.host_len, hi, a.S);
     for (int s = 0; s < a.P; ++s) {
       const int blk = (hi - s + a.P) % a.P;
       const int kbeg = blk * a.S;
@@ -119,6 +125,8 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32)
         if (blk > hi) continue;
         kend = min(kend, i + 1);
       }
+      if (a.host_len) kend = min(kend, kbeg + clamp_len(a.host_len, blk, a.S));
+      if (padded) break;  // padded query rows: O = 0, LSE = -inf
       simt_fwd_range<DPL>(q_sh[w], kbase, vbase, kv_row_stride, kbeg, kend, a.scale, m, l,
                           o);
     }
@@ -178,7 +186,8 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32) simt_bwd_dq_kernel(const 
 #pragma unroll
   for (int t = 0; t < DPL; ++t) dq[t] = 0.f;
   const int hi = i / a.S;
-  for (int s = 0; s < a.P; ++s) {
+  const bool padded = a.host_len && (i - hi * a.S) >= clamp_len(a.host_len, hi, a.S);
+  for (int s = 0; s < a.P && !padded; ++s) {
     const int blk = (hi - s + a.P) % a.P;
     const int kbeg = blk * a.S;
     int kend = kbeg + a.S;
@@ -188,6 +197,7 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32) simt_bwd_dq_kernel(const 
       if (blk > hi) continue;
       kend = min(kend, i + 1);
     }
+    if (a.host_len) kend = min(kend, kbeg + clamp_len(a.host_len, blk, a.S));
     for (int c = kbeg; c < kend; c += 32) {
       const int j = c + lane;
       float ds = 0.f;
@@ -243,7 +253,8 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32) simt_bwd_dkdv_kernel(cons
 #pragma unroll
   for (int t = 0; t < DPL; ++t) dk[t] = dv[t] = 0.f;
   const int hj = j / a.S;
-  for (int hh = 0; hh < group; ++hh) {
+  const bool padded = a.host_len && (j - hj * a.S) >= clamp_len(a.host_len, hj, a.S);
+  for (int hh = 0; hh < group && !padded; ++hh) {
     const int h = g * group + hh;
     const float* qbase = a.q + b * a.q_bs + (long long)h * D;
     const float* dobase = a.dO + b * a.q_bs + (long long)h * D;
@@ -252,6 +263,8 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32) simt_bwd_dkdv_kernel(cons
       const int host = (hj + s) % a.P;
       int qbeg = host * a.S;
       const int qend = qbeg + a.S;
+      int qlim = qend;
+      if (a.host_len) qlim = host * a.S + clamp_len(a.host_len, host, a.S);
       if (a.causal && a.striped) {
         // striped rows: local query row lq sees this key iff lq > lj, or
         // lq == lj and the key's host is not after the query's
@@ -260,10 +273,10 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32) simt_bwd_dkdv_kernel(cons
         if (host < hj) continue;
         qbeg = max(qbeg, j);
       }
-      for (int c = qbeg; c < qend; c += 32) {
+      for (int c = qbeg; c < qlim; c += 32) {
         const int i = c + lane;
         float p = 0.f, ds = 0.f;
-        if (i < qend) {
+        if (i < qlim) {
           const float lse = a.lse[sbase + i];
           if (lse != -INFINITY) {
             const float* qr = qbase + (long long)i * qrs;
@@ -278,7 +291,7 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32) simt_bwd_dkdv_kernel(cons
             ds = p * (dpacc - a.Dvec[sbase + i]);
           }
         }
-        const int cnt = min(32, qend - c);
+        const int cnt = min(32, qlim - c);
         for (int ii = 0; ii < cnt; ++ii) {
           const float pi = __shfl_sync(0xffffffffu, p, ii);
           const float dsi = __shfl_sync(0xffffffffu, ds, ii);
@@ -424,6 +437,22 @@ __global__ void f32_to_kernel(const float* __restrict__ src, void* out, int out_
   }
 }
 
+// One warp per (b, row): zero padded rows, set their LSE to -inf.
+__global__ void fill_padding_kernel(void* t, int dtype, long long bs, int B, int N, int H, int d,
+                                    int P, const int* host_len, float* lse) {
+  const long long row = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (row >= (long long)B * N) return;
+  const int n = (int)(row % N), b = (int)(row / N);
+  const int S = N / P;
+  const int host = n / S;
+  if (n - host * S < clamp_len(host_len, host, S)) return;
+  const long long base = b * bs + (long long)n * H * d;
+  for (int c = lane; c < H * d; c += 32) store_dtype(t, dtype, base + c, 0.f);
+  if (lse)
+    for (int h = lane; h < H; h += 32) lse[((long long)b * H + h) * N + n] = -INFINITY;
+}
+
 // One CTA waits on an mbarrier that nothing will ever arrive at; the bounded
 // wait must give up, record RA_ERR_TIMEOUT and let the kernel return.
 __global__ void selftest_timeout_kernel(unsigned long long limit_ns, int* status) {
@@ -545,6 +574,14 @@ cudaError_t launch_f32_to(const float* src, void* out, int out_dtype, long long 
                           long long epb, float mul, cudaStream_t st) {
   f32_to_kernel<<<grid_for(epb * B, 256 * 8), 256, 0, st>>>(src, out, out_dtype, out_bs, B,
                                                              epb, mul);
+  count_launch();
+  return cudaGetLastError();
+}
+
+cudaError_t launch_fill_padding(void* t, int dtype, long long bs, int B, int N, int H, int d, int P,
+                                const int* host_len, float* lse, cudaStream_t st) {
+  fill_padding_kernel<<<grid_for((long long)B * N, 8), 256, 0, st>>>(t, dtype, bs, B, N, H, d, P, host_len,
+                                                                      lse);
   count_launch();
   return cudaGetLastError();
 }

@@ -205,6 +205,26 @@ int ra_ring_fwd_noalloc(const void* q, const void* k, const void* v, ra_dtype dt
                         ra_shape shape, int P, int flags, float scale, void* o,
                         ra_dtype o_dtype, float* lse, void* stream);
 
+/* Ring forward / backward with variable per-host lengths ("FAQ" of "Ring
+ * Attention: Train 1M Tokens on 8GB GPUs in 2026": instead of computing on
+ * padding, each host tracks which of its positions are valid and masks the
+ * scores).  host_len is a device array of P int32: host i's first
+ * host_len[i] rows (of S = N/P) hold its tokens, the rest is padding (values
+ * are clamped to [0, S]).  The sequence is the valid rows in order, so a
+ * causal mask keeps its block structure; padded keys are never visible,
+ * padded query rows give O = 0, LSE = -inf, and padded rows get zero dQ, dK,
+ * dV.  Key/value tiles or query tiles wholly in padding are skipped.  Other
+ * arguments as in ra_ring_fwd / ra_ring_bwd; RA_STRIPED is not accepted. */
+int ra_ring_fwd_varlen(const void* q, const void* k, const void* v, ra_dtype dtype,
+                       ra_shape shape, int P, const int* host_len, int flags, float scale,
+                       void* o, ra_dtype o_dtype, float* lse, void* workspace,
+                       size_t ws_bytes, void* stream);
+int ra_ring_bwd_varlen(const void* q, const void* k, const void* v, const void* o,
+                       ra_dtype o_dtype, const void* dO, const float* lse, ra_dtype dtype,
+                       ra_shape shape, int P, const int* host_len, int flags, float scale,
+                       void* dq, void* dk, void* dv, ra_dtype grad_dtype, void* workspace,
+                       size_t ws_bytes, void* stream);
+
 /* Synchronise `stream`, then return and clear the device status word
  * (RA_OK, RA_ERR_RANGE or RA_ERR_TIMEOUT), or RA_ERR_CUDA if the stream
  * itself reports an error. */

@@ -9,6 +9,8 @@ from .attention import (  # noqa: F401
     attention_probs,
     attention_bwd,
     attention_rows,
+    attention_varlen,
+    varlen_rows,
     block_state,
     merge_states,
     finalize_state,

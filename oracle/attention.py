@@ -338,6 +338,37 @@ def ring_fwd_blocked_striped(q, k, v, P, scale):
     return O, LSE
 
 
+def varlen_rows(N, P, host_len):
+    """Rows holding real tokens when host i of P (S = N/P rows each) has only
+    its first host_len[i] rows valid and the rest is padding ("FAQ" of "Ring
+    Attention: Train 1M Tokens on 8GB GPUs in 2026": each host tracks which
+    positions are valid and masks the scores instead of computing on padding).
+    The valid rows, in order, are the sequence."""
+    S = N // P
+    return np.concatenate([np.arange(i * S, i * S + int(host_len[i])) for i in range(P)]).astype(np.int64)
+
+
+def attention_varlen(q, k, v, do, P, host_len, causal, scale):
+    """Exact attention (and, with dO given, its gradients) over the valid rows
+    only; padded rows get O = 0, LSE = -inf and zero gradients.  Returns
+    (O, LSE) or (dQ, dK, dV, O, LSE) in the padded layout."""
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    B, N, hq, d = q.shape
+    rows = varlen_rows(N, P, host_len)
+    O = np.zeros_like(q)
+    LSE = np.full((B, hq, N), NEG_INF)
+    if do is None:
+        Ov, Lv = attention_fwd(q[:, rows], k[:, rows], v[:, rows], causal, scale)
+        O[:, rows] = Ov
+        LSE[:, :, rows] = Lv
+        return O, LSE
+    dq, dk, dv = np.zeros_like(q), np.zeros_like(k), np.zeros_like(v)
+    gq, gk, gv, Ov, Lv, _ = attention_bwd(q[:, rows], k[:, rows], v[:, rows], _f64(do)[:, rows], causal, scale)
+    O[:, rows], LSE[:, :, rows] = Ov, Lv
+    dq[:, rows], dk[:, rows], dv[:, rows] = gq, gk, gv
+    return dq, dk, dv, O, LSE
+
+
 def ring_fwd_blocked(q, k, v, P, causal, scale):
     """Forward pass as the ring computes it: host i starts from the empty
     triple and, in ring order, merges the partial result of its queries

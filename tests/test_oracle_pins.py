@@ -341,3 +341,42 @@ def test_striped_blocks_share_the_causal_work_evenly():
     for i in range(P):
         for j in range(P):
             assert counts[i][j] == (S * (S + 1) // 2 if j <= i else S * (S - 1) // 2)
+
+
+# --- variable per-host lengths (dynamic masking) ---------------------------------
+
+def test_varlen_rows_concatenate_valid_prefixes():
+    rows = oracle.varlen_rows(12, 3, [2, 4, 0])
+    assert list(rows) == [0, 1, 4, 5, 6, 7]
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_varlen_with_full_hosts_is_plain_attention(causal):
+    q, k, v, do = rand(1, 12, 2, 4), rand(1, 12, 2, 4), rand(1, 12, 2, 4), rand(1, 12, 2, 4)
+    a = oracle.attention_varlen(q, k, v, do, 3, [4, 4, 4], causal, 0.5)
+    b = oracle.attention_bwd(q, k, v, do, causal, 0.5)
+    for x, y in zip(a, b[:5]):
+        np.testing.assert_allclose(x, y, atol=1e-13)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_varlen_ignores_padding_values_and_zeroes_padded_rows(causal):
+    P, S = 3, 5
+    lens = [3, 5, 1]
+    q, k, v, do = rand(1, P * S, 2, 4), rand(1, P * S, 1, 4), rand(1, P * S, 1, 4), rand(1, P * S, 2, 4)
+    rows = oracle.varlen_rows(P * S, P, lens)
+    pad = np.setdiff1d(np.arange(P * S), rows)
+    dq, dk, dv, O, L = oracle.attention_varlen(q, k, v, do, P, lens, causal, 0.7)
+    # padded rows: nothing computed, nothing leaks out
+    assert (O[:, pad] == 0).all() and np.isneginf(L[:, :, pad]).all()
+    assert (dq[:, pad] == 0).all() and (dk[:, pad] == 0).all() and (dv[:, pad] == 0).all()
+    # changing what sits in the padding changes nothing
+    q2, k2, v2, do2 = q.copy(), k.copy(), v.copy(), do.copy()
+    for t in (q2, k2, v2, do2):
+        t[:, pad] = 1e3 * rand(*t[:, pad].shape)
+    res2 = oracle.attention_varlen(q2, k2, v2, do2, P, lens, causal, 0.7)
+    for x, y in zip((dq, dk, dv, O, L), res2):
+        np.testing.assert_allclose(x, y, atol=1e-12)
+    # the valid rows are exactly attention over the packed sequence (brute force)
+    Op, Lp = oracle.attention_fwd(q[:, rows], k[:, rows], v[:, rows], causal, 0.7)
+    np.testing.assert_allclose(O[:, rows], Op, atol=1e-13)
