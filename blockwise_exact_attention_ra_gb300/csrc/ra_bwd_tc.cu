@@ -91,6 +91,17 @@ __device__ __forceinline__ int host_len_at(const int* hl, int j, int S);
 
 template <bool STRIPED, bool VARLEN>
 __device__ __forceinline__ BwdUnit bwd_unit(const TcBwdArgs& a, int u) {
+  // CTA b takes units b, b + G, b + 2G, ... (G CTAs).  Odd rounds run in
+  // reverse, so the CTA that drew the heaviest unit of one round draws the
+  // lightest of the next: every CTA gets the same work per pair of rounds and
+  // they sweep the same head together, keeping its Q, dO and dQ lines in L2.
+  {
+    const int G = gridDim.x, rnd = u / G;
+    if (rnd & 1) {
+      const int in_round = min(G, a.num_units - rnd * G);
+      u = rnd * G + (in_round - 1 - (u - rnd * G));
+    }
+  }
   BwdUnit r;
   const int nT = a.N / 128;
   const int bg = u / nT;
