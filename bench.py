@@ -329,46 +329,53 @@ def run_ours(args, ws, rank, local):
                    "tflops": (fwd_fl + bwd_fl) / ((f_ms + b_ms) * 1e-3) / 1e12,
                    "fwd_tflops": fwd_fl / (f_ms * 1e-3) / 1e12, "bwd_tflops": bwd_fl / (b_ms * 1e-3) / 1e12}
 
-    # end to end through the public API with pinned host buffers
+    # end to end through the public C-ABI call with host buffers: every step
+    # uploads its q, k, v, dO from pinned host memory and downloads O, LSE, dQ,
+    # dK, dV (bf16) to pinned host memory.  Steps alternate between two streams
+    # and two workspaces so that one step's copies overlap the other's kernels.
     e2e = None
     if not args.no_e2e:
-        hq = [t.to("cpu").pin_memory() for t in (q, k, v, do)]
-        dq_ = [torch.empty_like(t) for t in (q, k, v, do)]
-        o16 = torch.empty(B, N, Hq, d, dtype=torch.bfloat16, device=dev)
-        g16 = [torch.empty(B, N, Hq, d, dtype=torch.bfloat16, device=dev),
-               torch.empty(B, N, Hkv, d, dtype=torch.bfloat16, device=dev),
-               torch.empty(B, N, Hkv, d, dtype=torch.bfloat16, device=dev)]
-        wsb16 = torch.empty(max(16, ra.ra_ring_bwd_workspace_bytes(ra.RA_BF16, ra.RA_BF16, sh, P)),
-                            dtype=torch.uint8, device=dev)
-        host_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in [o16] + g16]
+        host_in = [t.to("cpu").pin_memory() for t in (q, k, v, do)]
+        host_out = [[torch.empty(B, N, Hq, d, dtype=torch.bfloat16, pin_memory=True),
+                     torch.empty(B, Hq, N, dtype=torch.float32, pin_memory=True),
+                     torch.empty(B, N, Hq, d, dtype=torch.bfloat16, pin_memory=True),
+                     torch.empty(B, N, Hkv, d, dtype=torch.bfloat16, pin_memory=True),
+                     torch.empty(B, N, Hkv, d, dtype=torch.bfloat16, pin_memory=True)] for _ in range(2)]
+        hws = ra.ra_ring_step_host_workspace_bytes(ra.RA_BF16, ra.RA_BF16, ra.RA_BF16, sh, P)
+        wsh = [torch.empty(hws, dtype=torch.uint8, device=dev) for _ in range(2)]
+        sts = [torch.cuda.Stream(dev), torch.cuda.Stream(dev)]
 
-        def e2e_step():
-            for h, dd in zip(hq, dq_):
-                dd.copy_(h, non_blocking=True)
-            ra.ra_ring_fwd(dq_[0], dq_[1], dq_[2], P, True, scale, o16, lse, wsf, stream)
-            ra.ra_ring_bwd(dq_[0], dq_[1], dq_[2], o16, dq_[3], lse, P, True, scale, g16[0], g16[1], g16[2],
-                           wsb16, stream)
-            for dst, src in zip(host_out, [o16] + g16):
-                dst.copy_(src, non_blocking=True)
+        def e2e_steps(n):
+            for i in range(n):
+                ra.ra_ring_step_host(*host_in, P, True, scale, *host_out[i % 2], wsh[i % 2], sts[i % 2])
 
-        for _ in range(max(1, args.warmup)):
-            e2e_step()
+        main = torch.cuda.current_stream(dev)
+        for st_ in sts:
+            st_.wait_stream(main)
+        e2e_steps(max(1, args.warmup))
+        for st_ in sts:
+            main.wait_stream(st_)
         torch.cuda.synchronize(dev)
         if ws > 1:
             torch.distributed.barrier()
         a = torch.cuda.Event(enable_timing=True)
         b = torch.cuda.Event(enable_timing=True)
-        a.record(stream)
-        for _ in range(args.steps):
-            e2e_step()
-        b.record(stream)
+        a.record(main)
+        for st_ in sts:
+            st_.wait_event(a)
+        e2e_steps(args.steps)
+        for st_ in sts:
+            main.wait_stream(st_)
+        b.record(main)
         torch.cuda.synchronize(dev)
-        ra.ra_sync_status(stream)
+        ra.ra_sync_status(main)
         e_ms = max_over_ranks(a.elapsed_time(b) / args.steps, dev)
         e2e = {"value": job_value(ws, fwd_fl + bwd_fl, e_ms), "unit": "TFLOP/s",
                "ms_per_step": e_ms,
-               "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in hq),
-               "d2h_bytes_per_step": sum(t.numel() * t.element_size() for t in host_out)}
+               "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in host_in),
+               "d2h_bytes_per_step": sum(t.numel() * t.element_size() for t in host_out[0]),
+               "api": "ra_ring_step_host (host buffers, pinned), two streams alternating"}
+        del wsh
 
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:

@@ -19,7 +19,8 @@ __all__ = [
     "RAError", "RaShape", "lib", "shape_of",
     "ra_acc_init", "ra_block_fwd", "ra_block_fwd_workspace_bytes", "ra_merge", "ra_finalize",
     "ra_ring_fwd", "ra_ring_fwd_workspace_bytes", "ra_ring_bwd", "ra_ring_bwd_workspace_bytes",
-    "ra_ring_fwd_noalloc", "ra_ring_fwd_varlen", "ra_ring_bwd_varlen",
+    "ra_ring_fwd_noalloc", "ra_ring_fwd_varlen", "ra_ring_bwd_varlen", "ra_ring_step_host",
+    "ra_ring_step_host_workspace_bytes",
     "ra_sync_status", "ra_last_error", "ra_launch_count", "ra_selftest_timeout",
     "ra_kernel_timing", "ra_kernel_timing_read",
     "ring_attention_fwd", "ring_attention_bwd", "RA_F32", "RA_BF16", "RA_F16",
@@ -68,6 +69,8 @@ def _load():
         "ra_ring_fwd_workspace_bytes": (sz, [i, sh, i]),
         "ra_ring_fwd_noalloc": (i, [vp, vp, vp, i, sh, i, i, f, vp, i, vp, vp]),
         "ra_ring_fwd_varlen": (i, [vp, vp, vp, i, sh, i, vp, i, f, vp, i, vp, vp, sz, vp]),
+        "ra_ring_step_host": (i, [vp, vp, vp, vp, i, sh, i, i, f, vp, i, vp, vp, vp, vp, i, vp, sz, vp]),
+        "ra_ring_step_host_workspace_bytes": (sz, [i, i, i, sh, i]),
         "ra_ring_bwd_varlen": (i, [vp, vp, vp, vp, i, vp, vp, i, sh, i, vp, i, f, vp, vp, vp, i, vp, sz, vp]),
         "ra_ring_bwd": (i, [vp, vp, vp, vp, i, vp, vp, i, sh, i, i, f, vp, vp, vp, i, vp, sz, vp]),
         "ra_ring_bwd_workspace_bytes": (sz, [i, i, sh, i]),
@@ -237,6 +240,34 @@ def ra_ring_bwd_varlen(q, k, v, o, dO, lse, P, host_len, causal, scale, dq, dk, 
                                   _dt(q), shape, int(P), _ptr(host_len), _flags(causal, precise),
                                   float(scale), _ptr(dq), _ptr(dk), _ptr(dv), _dt(dq), _ptr(workspace),
                                   ws_bytes, _stream(stream)))
+
+
+def ra_ring_step_host_workspace_bytes(dtype, o_dtype, grad_dtype, shape, P):
+    return int(lib.ra_ring_step_host_workspace_bytes(dtype, o_dtype, grad_dtype, shape, int(P)))
+
+
+def ra_ring_step_host(q, k, v, dO, P, causal, scale, o, lse, dq, dk, dv, workspace, stream=None,
+                      precise=False, striped=False):
+    """Forward + backward with q, k, v, dO and the outputs o, lse, dq, dk, dv in
+    host (CPU) memory; the library uploads, computes and downloads on `stream`
+    (pinned tensors make the copies asynchronous).  workspace: device uint8
+    tensor of ra_ring_step_host_workspace_bytes() bytes."""
+    for t in (q, k, v, dO, o, lse, dq, dk, dv):
+        if t.is_cuda:
+            raise RAError(1, "ra_ring_step_host takes host tensors")
+    # one batch stride per group: q's for dO, o, dq; k's for v, dk, dv
+    for t, ref in ((dO, q), (o, q), (dq, q), (v, k), (dk, k), (dv, k)):
+        _check_layout(t, "a host tensor")
+        if t.shape != ref.shape or (t.dim() == 4 and _bstride(t) != _bstride(ref)):
+            raise RAError(1, "ra_ring_step_host: a tensor's shape or batch stride differs from its group's")
+    if not lse.is_contiguous():
+        raise RAError(1, "ra_ring_step_host: lse must be packed [B, Hq, N]")
+    shape = shape_of(q, k)
+    ws_bytes = workspace.numel() * workspace.element_size()
+    _check(lib.ra_ring_step_host(_ptr(q), _ptr(k), _ptr(v), _ptr(dO), _dt(q), shape, int(P),
+                                 _flags(causal, precise, striped), float(scale), _ptr(o), _dt(o),
+                                 _ptr(lse), _ptr(dq), _ptr(dk), _ptr(dv), _dt(dq), _ptr(workspace),
+                                 ws_bytes, _stream(stream)))
 
 
 def ra_ring_bwd_workspace_bytes(dtype, grad_dtype, shape, P):

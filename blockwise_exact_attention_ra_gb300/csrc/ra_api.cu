@@ -722,4 +722,196 @@ int ra_ring_bwd_varlen(const void* q, const void* k, const void* v, const void* 
                        grad_dtype, workspace, ws_bytes, stream, host_len);
 }
 
+#pragma GCC visibility pop
+}  // extern "C"
+
+// ----------------------------------------------------- one step from host memory
+namespace ra {
+namespace {
+
+// Device workspace of ra_ring_step_host: device copies of the inputs and
+// outputs (packed [B, N, H, d]; LSE [B, Hq, N]) and the forward and backward
+// workspaces.
+struct HostWs {
+  size_t q, k, v, dO, o, lse, dq, dk, dv, fwd, bwd, total;
+};
+HostWs host_layout(int dtype, int o_dtype, int grad_dtype, const ra_shape& sh, int P) {
+  HostWs w{};
+  const size_t qel = (size_t)sh.B * sh.N_q * sh.Hq * sh.d, kvel = (size_t)sh.B * sh.N_kv * sh.Hkv * sh.d;
+  ra_shape packed = sh;
+  packed.q_bstride = 0;
+  packed.kv_bstride = 0;
+  size_t off = 0;
+  auto take = [&off](size_t bytes) {
+    const size_t at = off;
+    off += align256(bytes);
+    return at;
+  };
+  const size_t es = dtype_size(dtype), gs = dtype_size(grad_dtype);
+  w.q = take(qel * es);
+  w.k = take(kvel * es);
+  w.v = take(kvel * es);
+  w.dO = take(qel * es);
+  w.o = take(qel * dtype_size(o_dtype));
+  w.lse = take((size_t)sh.B * sh.Hq * sh.N_q * 4);
+  w.dq = take(qel * gs);
+  w.dk = take(kvel * gs);
+  w.dv = take(kvel * gs);
+  w.fwd = take(ra_ring_fwd_workspace_bytes((ra_dtype)dtype, packed, P));
+  w.bwd = take(ra_ring_bwd_workspace_bytes((ra_dtype)dtype, (ra_dtype)grad_dtype, packed, P));
+  w.total = off;
+  return w;
+}
+
+// Side streams of ra_ring_step_host, one pair per device, created on first
+// use and kept for the life of the process.
+struct SideStreams {
+  std::mutex mu;
+  cudaStream_t in[kMaxDevices] = {}, out[kMaxDevices] = {};
+};
+SideStreams& side_streams() {
+  static SideStreams s;
+  return s;
+}
+int get_side_streams(cudaStream_t* in, cudaStream_t* out) {
+  int dev;
+  int rc = current_device(&dev);
+  if (rc) return rc;
+  SideStreams& s = side_streams();
+  std::lock_guard<std::mutex> lk(s.mu);
+  if (!s.in[dev]) {
+    cudaError_t e = cudaStreamCreateWithFlags(&s.in[dev], cudaStreamNonBlocking);
+    if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&s.out[dev], cudaStreamNonBlocking);
+    if (e != cudaSuccess) {
+      s.in[dev] = s.out[dev] = nullptr;
+      return cuda_fail(e, "create side streams");
+    }
+  }
+  *in = s.in[dev];
+  *out = s.out[dev];
+  return RA_OK;
+}
+
+// Copies B batches of `batch` elements between a buffer with batch stride
+// `src_bs` and one with batch stride `dst_bs` (elements of `es` bytes).
+cudaError_t copy_batches(void* dst, long long dst_bs, const void* src, long long src_bs, int B,
+                         long long batch, size_t es, cudaStream_t st) {
+  if (dst_bs == batch && src_bs == batch)
+    return cudaMemcpyAsync(dst, src, (size_t)B * batch * es, cudaMemcpyDefault, st);
+  for (int b = 0; b < B; ++b) {
+    cudaError_t e = cudaMemcpyAsync(static_cast<char*>(dst) + (size_t)b * dst_bs * es,
+                                    static_cast<const char*>(src) + (size_t)b * src_bs * es,
+                                    (size_t)batch * es, cudaMemcpyDefault, st);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
+}
+
+struct Events {
+  cudaEvent_t e[4] = {};
+  ~Events() {
+    for (cudaEvent_t x : e)
+      if (x) cudaEventDestroy(x);  // released once the recorded work completes
+  }
+};
+
+}  // namespace
+}  // namespace ra
+
+extern "C" {
+#pragma GCC visibility push(default)
+
+size_t ra_ring_step_host_workspace_bytes(ra_dtype dtype, ra_dtype o_dtype, ra_dtype grad_dtype,
+                                         ra_shape shape, int P) {
+  if (shape.B < 1 || shape.N_q < 1 || shape.N_kv < 1 || shape.Hq < 1 || shape.Hkv < 1 || shape.d < 1 ||
+      !valid_dtype(dtype) || !valid_dtype(o_dtype) || !valid_dtype(grad_dtype))
+    return 0;
+  return host_layout(dtype, o_dtype, grad_dtype, shape, P).total;
+}
+
+int ra_ring_step_host(const void* q, const void* k, const void* v, const void* dO, ra_dtype dtype,
+                      ra_shape shape, int P, int flags, float scale, void* o, ra_dtype o_dtype,
+                      float* lse, void* dq, void* dk, void* dv, ra_dtype grad_dtype, void* workspace,
+                      size_t ws_bytes, void* stream) {
+  // everything the forward and backward would reject is rejected before any
+  // copy is enqueued
+  if (flags & ~(RA_CAUSAL | RA_PRECISE | RA_STRIPED))
+    return fail(RA_ERR_INVALID_ARG, "unknown flag bits 0x%x", flags);
+  Shape s;
+  int rc;
+  if ((rc = check_shape(shape, &s))) return rc;
+  if (!valid_dtype(dtype) || !valid_dtype(o_dtype) || !valid_dtype(grad_dtype))
+    return fail(RA_ERR_INVALID_ARG, "bad dtype");
+  if ((rc = check_scale(scale))) return rc;
+  if ((rc = check_ring(s, P, dtype))) return rc;
+  const void* ins[4] = {q, k, v, dO};
+  const char* in_names[4] = {"q", "k", "v", "dO"};
+  for (int i = 0; i < 4; ++i)
+    if (!ins[i]) return fail(RA_ERR_INVALID_ARG, "%s is NULL", in_names[i]);
+  if (!o || !lse || !dq || !dk || !dv) return fail(RA_ERR_INVALID_ARG, "an output pointer is NULL");
+  const HostWs w = host_layout(dtype, o_dtype, grad_dtype, shape, P);
+  if (!workspace || ws_bytes < w.total)
+    return fail(RA_ERR_INVALID_ARG, "workspace of %zu bytes needed (got %zu)", w.total, ws_bytes);
+  if (reinterpret_cast<uintptr_t>(workspace) & 255u)
+    return fail(RA_ERR_INVALID_ARG, "workspace is not 256-byte aligned");
+  int* st;
+  if ((rc = status_ptr(&st))) return rc;
+  if (dtype == RA_F32) {
+    if (s.d != 32 && s.d != 64 && s.d != 128)
+      return fail(RA_ERR_UNSUPPORTED, "fp32 path supports d in {32, 64, 128} (got %d)", s.d);
+  } else {
+    Shape packed = s;
+    packed.q_bs = (long long)s.Nq * s.Hq * s.d;
+    packed.kv_bs = (long long)s.Nkv * s.Hkv * s.d;
+    if ((rc = check_tc(packed, dtype))) return rc;
+  }
+  cudaStream_t main_st = static_cast<cudaStream_t>(stream), in_st, out_st;
+  if ((rc = get_side_streams(&in_st, &out_st))) return rc;
+  Events ev;
+  for (cudaEvent_t& e : ev.e) {
+    cudaError_t err = cudaEventCreateWithFlags(&e, cudaEventDisableTiming);
+    if (err != cudaSuccess) return cuda_fail(err, "cudaEventCreateWithFlags");
+  }
+  char* ws = static_cast<char*>(workspace);
+  const long long qel = (long long)s.Nq * s.Hq * s.d, kvel = (long long)s.Nkv * s.Hkv * s.d;
+  const size_t es = dtype_size(dtype), gs = dtype_size(grad_dtype);
+  ra_shape packed = shape;
+  packed.q_bstride = 0;
+  packed.kv_bstride = 0;
+  cudaError_t e;
+  // dO travels on the input side stream while q, k, v go up and the forward runs
+  if ((e = cudaEventRecord(ev.e[0], main_st)) != cudaSuccess ||
+      (e = cudaStreamWaitEvent(in_st, ev.e[0], 0)) != cudaSuccess ||
+      (e = copy_batches(ws + w.dO, qel, dO, s.q_bs, s.B, qel, es, in_st)) != cudaSuccess ||
+      (e = cudaEventRecord(ev.e[1], in_st)) != cudaSuccess)
+    return cuda_fail(e, "dO upload");
+  if ((e = copy_batches(ws + w.q, qel, q, s.q_bs, s.B, qel, es, main_st)) != cudaSuccess ||
+      (e = copy_batches(ws + w.k, kvel, k, s.kv_bs, s.B, kvel, es, main_st)) != cudaSuccess ||
+      (e = copy_batches(ws + w.v, kvel, v, s.kv_bs, s.B, kvel, es, main_st)) != cudaSuccess)
+    return cuda_fail(e, "q, k, v upload");
+  rc = ring_fwd_impl(ws + w.q, ws + w.k, ws + w.v, dtype, packed, P, flags, scale, ws + w.o, o_dtype,
+                     reinterpret_cast<float*>(ws + w.lse), ws + w.fwd, w.bwd - w.fwd, stream, nullptr);
+  if (rc) return rc;
+  // O and LSE travel down on the output side stream while the backward runs
+  if ((e = cudaEventRecord(ev.e[2], main_st)) != cudaSuccess ||
+      (e = cudaStreamWaitEvent(out_st, ev.e[2], 0)) != cudaSuccess ||
+      (e = copy_batches(o, s.q_bs, ws + w.o, qel, s.B, qel, dtype_size(o_dtype), out_st)) != cudaSuccess ||
+      (e = cudaMemcpyAsync(lse, ws + w.lse, (size_t)s.B * s.Hq * s.Nq * 4, cudaMemcpyDefault, out_st)) !=
+          cudaSuccess ||
+      (e = cudaEventRecord(ev.e[3], out_st)) != cudaSuccess)
+    return cuda_fail(e, "O, LSE download");
+  if ((e = cudaStreamWaitEvent(main_st, ev.e[1], 0)) != cudaSuccess) return cuda_fail(e, "join dO upload");
+  rc = ring_bwd_impl(ws + w.q, ws + w.k, ws + w.v, ws + w.o, o_dtype, ws + w.dO,
+                     reinterpret_cast<const float*>(ws + w.lse), dtype, packed, P, flags, scale, ws + w.dq,
+                     ws + w.dk, ws + w.dv, grad_dtype, ws + w.bwd, w.total - w.bwd, stream, nullptr);
+  if (rc) return rc;
+  if ((e = copy_batches(dq, s.q_bs, ws + w.dq, qel, s.B, qel, gs, main_st)) != cudaSuccess ||
+      (e = copy_batches(dk, s.kv_bs, ws + w.dk, kvel, s.B, kvel, gs, main_st)) != cudaSuccess ||
+      (e = copy_batches(dv, s.kv_bs, ws + w.dv, kvel, s.B, kvel, gs, main_st)) != cudaSuccess)
+    return cuda_fail(e, "gradient download");
+  if ((e = cudaStreamWaitEvent(main_st, ev.e[3], 0)) != cudaSuccess) return cuda_fail(e, "join O download");
+  return RA_OK;
+}
+
+#pragma GCC visibility pop
 }  // extern "C"

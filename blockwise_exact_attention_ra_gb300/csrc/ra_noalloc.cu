@@ -64,4 +64,5 @@ int ra_ring_fwd_noalloc(const void* q, const void* k, const void* v, ra_dtype dt
                      kScratchBytes, stream);
 }
 
+#pragma GCC visibility pop
 }  // extern "C"

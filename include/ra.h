@@ -225,6 +225,37 @@ int ra_ring_bwd_varlen(const void* q, const void* k, const void* v, const void* 
                        void* dq, void* dk, void* dv, ra_dtype grad_dtype, void* workspace,
                        size_t ws_bytes, void* stream);
 
+/* One forward + backward step with the tensors in HOST memory: the work of
+ * ra_ring_fwd followed by ra_ring_bwd, with the uploads and downloads it
+ * needs.  The pages keep every block resident on its host and only move KV
+ * between hosts; this call is for callers whose batches live in host memory
+ * (a data loader, a CPU-side training loop).
+ *   Inputs q, dO [B,N,Hq,d] and k, v [B,N,Hkv,d] in dtype; outputs o (o_dtype),
+ *   lse [B,Hq,N] fp32 (packed), dq, dk, dv (grad_dtype); batch strides from
+ *   `shape` apply to the host buffers.  All ten pointers are host pointers.
+ *   workspace: device memory, 256-byte aligned, at least
+ *   ra_ring_step_host_workspace_bytes() bytes; it holds the device copies and
+ *   the forward and backward workspaces.
+ *   Order: on `stream`, q, k, v go up, the forward runs, the backward runs,
+ *   dq, dk, dv come down.  dO goes up on a library-owned side stream while the
+ *   forward runs, and o and lse come down on a second one while the backward
+ *   runs; both are joined back into `stream` with events, so the outputs are
+ *   complete once `stream` has completed.  Pinned host memory (cudaHostAlloc,
+ *   cudaHostRegister) makes every copy asynchronous; pageable memory works,
+ *   but the copies then block the calling thread.  Two calls on two streams
+ *   with two workspaces overlap one step's copies with the other's kernels.
+ *   The workspace must not be in use by work that is not ordered before this
+ *   call on `stream`.  The side streams are created on the first call on
+ *   each device (make that call before any stream capture).
+ *   Errors: everything ra_ring_fwd or ra_ring_bwd would reject is rejected
+ *   before anything is enqueued; flags as for ra_ring_fwd. */
+int ra_ring_step_host(const void* q, const void* k, const void* v, const void* dO,
+                      ra_dtype dtype, ra_shape shape, int P, int flags, float scale,
+                      void* o, ra_dtype o_dtype, float* lse, void* dq, void* dk, void* dv,
+                      ra_dtype grad_dtype, void* workspace, size_t ws_bytes, void* stream);
+size_t ra_ring_step_host_workspace_bytes(ra_dtype dtype, ra_dtype o_dtype,
+                                         ra_dtype grad_dtype, ra_shape shape, int P);
+
 /* Synchronise `stream`, then return and clear the device status word
  * (RA_OK, RA_ERR_RANGE or RA_ERR_TIMEOUT), or RA_ERR_CUDA if the stream
  * itself reports an error. */

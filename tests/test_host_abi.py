@@ -85,5 +85,31 @@ def test_null_and_misaligned_pointers_are_rejected(ra):
     assert lib.ra_block_fwd(vp, vp, vp, ra.RA_BF16, vp, vp, vp, sh, -1, 0, 1, 0.1, None, 0, None) == 1
 
 
+def test_host_step_workspace_and_validation(ra):
+    lib = ra.lib
+    sh = ra.RaShape(2, 1024, 1024, 4, 2, 128, 0, 0)
+    qel, kvel = 2 * 1024 * 4 * 128, 2 * 1024 * 2 * 128
+    ws = ra.ra_ring_step_host_workspace_bytes(ra.RA_BF16, ra.RA_BF16, ra.RA_F32, sh, 4)
+    # device copies (q, k, v, dO bf16; O bf16; LSE; dq, dk, dv fp32) + fwd and bwd workspaces
+    copies = 2 * (2 * qel + 2 * kvel) + 2 * qel + 4 * 2 * 4 * 1024 + 4 * (qel + 2 * kvel)
+    need = copies + ra.ra_ring_fwd_workspace_bytes(ra.RA_BF16, sh, 4) + \
+        ra.ra_ring_bwd_workspace_bytes(ra.RA_BF16, ra.RA_F32, sh, 4)
+    assert need <= ws <= need + 16 * 256
+    assert ra.ra_ring_step_host_workspace_bytes(9, ra.RA_BF16, ra.RA_F32, sh, 4) == 0
+    vp = ctypes.c_void_p(4096)
+    wsz = ctypes.c_size_t(ws)
+
+    def call(*, q=vp, flags=1, P=4, o=vp, workspace=vp, nbytes=wsz, shape=sh):
+        return lib.ra_ring_step_host(q, vp, vp, vp, ra.RA_BF16, shape, P, flags, 0.1, o, ra.RA_BF16, vp,
+                                     vp, vp, vp, ra.RA_F32, workspace, nbytes, None)
+    assert call(flags=8) == 1 and "flag" in ra.ra_last_error()
+    assert call(P=3) == 1
+    assert call(q=None) == 1 and "q" in ra.ra_last_error()
+    assert call(o=None) == 1
+    assert call(nbytes=ctypes.c_size_t(ws - 1)) == 1 and "workspace" in ra.ra_last_error()
+    assert call(workspace=ctypes.c_void_p(4096 + 16)) == 1 and "aligned" in ra.ra_last_error()
+    assert call(shape=ra.RaShape(2, 1024, 1024, 3, 2, 128, 0, 0)) == 1
+
+
 def test_launch_counter_is_readable(ra):
     assert isinstance(ra.ra_launch_count(), int) and ra.ra_launch_count() >= 0
