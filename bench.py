@@ -329,6 +329,48 @@ def run_ours(args, ws, rank, local):
                    "tflops": (fwd_fl + bwd_fl) / ((f_ms + b_ms) * 1e-3) / 1e12,
                    "fwd_tflops": fwd_fl / (f_ms * 1e-3) / 1e12, "bwd_tflops": bwd_fl / (b_ms * 1e-3) / 1e12}
 
+    # variable per-host lengths (dynamic masking): the same tensors through the
+    # varlen entry points, (a) with every host full, whose cost over the plain
+    # ring is the price of the masking, and (b) with seeded ragged lengths in
+    # [S/2, S], timed against the flops of causal attention over the valid tokens
+    varlen = None
+    if not args.no_varlen:
+        S = N // P
+        g = torch.Generator().manual_seed(4321 + rank)
+        ragged = torch.randint(S // 2, S + 1, (P,), generator=g, dtype=torch.int32)
+
+        def time_varlen(hl):
+            def one(ev=None):
+                ra.ra_ring_fwd_varlen(q, k, v, P, hl, True, scale, o, lse, wsf, stream)
+                if ev is not None:
+                    ev.record(stream)
+                ra.ra_ring_bwd_varlen(q, k, v, o, do, lse, P, hl, True, scale, dq, dk, dv, wsb, stream)
+            for _ in range(args.warmup):
+                one()
+            torch.cuda.synchronize(dev)
+            evs = [torch.cuda.Event(enable_timing=True) for _ in range(3 * args.steps)]
+            for s_ in range(args.steps):
+                evs[3 * s_].record(stream)
+                one(evs[3 * s_ + 1])
+                evs[3 * s_ + 2].record(stream)
+            torch.cuda.synchronize(dev)
+            ra.ra_sync_status(stream)
+            f = sum(evs[3 * i].elapsed_time(evs[3 * i + 1]) for i in range(args.steps)) / args.steps
+            b_ = sum(evs[3 * i + 1].elapsed_time(evs[3 * i + 2]) for i in range(args.steps)) / args.steps
+            return f, b_
+
+        full = torch.full((P,), S, dtype=torch.int32, device=dev)
+        f_ms, b_ms = time_varlen(full)
+        L = int(ragged.sum())
+        rf_ms, rb_ms = time_varlen(ragged.to(dev))
+        lf, lb = algo_flops(B, L, Hq, d)
+        varlen = {"full_lengths": {"tflops": (fwd_fl + bwd_fl) / ((f_ms + b_ms) * 1e-3) / 1e12,
+                                   "ms_per_step": f_ms + b_ms, "fwd_ms": f_ms, "bwd_ms": b_ms,
+                                   "overhead_vs_plain": (f_ms + b_ms) / (fwd_ms + bwd_ms) - 1.0},
+                  "ragged": {"host_len": "seeded uniform in [S/2, S] per host", "valid_tokens": L,
+                             "ms_per_step": rf_ms + rb_ms, "fwd_ms": rf_ms, "bwd_ms": rb_ms,
+                             "tflops_on_valid_tokens": (lf + lb) / ((rf_ms + rb_ms) * 1e-3) / 1e12}}
+
     # end to end through the public C-ABI call with host buffers: every step
     # uploads its q, k, v, dO from pinned host memory and downloads O, LSE, dQ,
     # dK, dV (bf16) to pinned host memory.  Steps alternate between two streams
@@ -396,7 +438,7 @@ def run_ours(args, ws, rank, local):
             "pct_of_peak": value / ws / peaks["sustained"],
             "fwd_ms": fwd_ms, "bwd_ms": bwd_ms,
             "fwd_tflops": fwd_fl / (fwd_ms * 1e-3) / 1e12, "bwd_tflops": bwd_fl / (bwd_ms * 1e-3) / 1e12,
-            "kernels": kern, "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "striped": striped,
+            "kernels": kern, "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "striped": striped, "varlen": varlen,
             "gpu_launches": launches, "clocks": clk,
         }
         print(json.dumps(line), flush=True)
@@ -413,6 +455,7 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-striped", action="store_true", help="skip the striped-layout measurement")
+    ap.add_argument("--no-varlen", action="store_true", help="skip the variable-length measurement")
     ap.add_argument("--cpu-rows", type=int, default=3072)
     ap.add_argument("--ref-rows", type=int, default=1024)
     ap.add_argument("--N", type=int, default=None, help="override N (profiling on a smaller case)")

@@ -457,10 +457,23 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
     bool ok = true;
     for (int u = blockIdx.x; u < a.num_units && ok; u += gridDim.x) {
       const BwdUnit bu = bwd_unit<STRIPED, VARLEN>(a, u);
+      // padding: key rows of this tile from kvalid on (variable host lengths)
+      int kvalid = 128;
+      if (VARLEN) {
+        const int T = a.ring_S / 128;
+        kvalid = host_len_at(a.host_len, bu.jt / T, a.ring_S) - (bu.jt % T) * 128;
+      }
       for (int it = 0; it < bu.n_iter; ++it, ++gi) {
         int h, qt;
         bwd_iter<STRIPED>(a, bu, it, &h, &qt);
-        if (VARLEN && !q_tile_valid<VARLEN>(a, qt)) { --gi; continue; }
+        // padding: query columns of this tile from qvalid on; a tile wholly in
+        // padding is skipped by every role
+        int qvalid = 128;
+        if (VARLEN) {
+          const int T = a.ring_S / 128;
+          qvalid = host_len_at(a.host_len, qt / T, a.ring_S) - (qt % T) * 128;
+          if (qvalid <= 0) { --gi; continue; }
+        }
         const int s = gi & 1;
         const float* lse2 = reinterpret_cast<const float*>(smem + L::kVec0 + s * 1024) + half * 64;
         const float* dvec = lse2 + 128;
@@ -476,14 +489,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
         // c visible to key row r iff c >= r); for a striped layout the same
         // local tile of any host pair, strict (c > r) when the key's host
         // comes after the query's
-        // padding: query columns from qvalid on, key rows from kvalid on
-        int qvalid = 128, kvalid = 128;
-        if (VARLEN) {
-          const int T = a.ring_S / 128;
-          qvalid = host_len_at(a.host_len, qt / T, a.ring_S) - (qt % T) * 128;
-          kvalid = host_len_at(a.host_len, bu.jt / T, a.ring_S) - (bu.jt % T) * 128;
-        }
-        const bool pad = qvalid < 128 || kvalid < 128;
+        const bool pad = VARLEN && (qvalid < 128 || kvalid < 128);
         bool diag;
         int strict = 0;
         if (STRIPED) {
@@ -493,18 +499,24 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
         } else {
           diag = a.causal && qt == bu.jt;
         }
-        // P^T = exp2(S^T * scale*log2e - LSE*log2e); query column c visible iff c >= key row
+        // P^T = exp2(S^T * scale*log2e - LSE*log2e)
 #pragma unroll
         for (int c = 0; c < 64; c += 4) {
           const float4 l4 = *reinterpret_cast<const float4*>(lse2 + c);
           const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
 #pragma unroll
-          for (int u4 = 0; u4 < 4; ++u4) {
-            float p = ex2_approx(fmaf(__uint_as_float(pr[c + u4]), sl2, -lv[u4]));
-            if (diag && half * 64 + c + u4 < r + strict) p = 0.f;
-            if (VARLEN && pad && (half * 64 + c + u4 >= qvalid || r >= kvalid)) p = 0.f;
-            pr[c + u4] = __float_as_uint(p);
-          }
+          for (int u4 = 0; u4 < 4; ++u4)
+            pr[c + u4] = __float_as_uint(ex2_approx(fmaf(__uint_as_float(pr[c + u4]), sl2, -lv[u4])));
+        }
+        // the masks, only on the tiles that have any: this half's columns below
+        // c_lo (causal) or from c_hi on (padded queries), and every column of
+        // a padded key row, are zero
+        if (diag || pad) {
+          const int c_lo = diag ? r + strict - half * 64 : 0;
+          const int c_hi = VARLEN ? (r < kvalid ? qvalid - half * 64 : 0) : 64;
+#pragma unroll
+          for (int c = 0; c < 64; ++c)
+            if (c < c_lo || c >= c_hi) pr[c] = 0u;
         }
         // P^T (fp16) back into TMEM for the dV MMA
 #pragma unroll

@@ -108,12 +108,16 @@ __device__ __forceinline__ int kt_at(const UnitInfo& u, int it, int* tk = nullpt
 
 // With variable host lengths a key/value tile wholly in a host's padding is
 // skipped by every role.
-__device__ __forceinline__ bool iter_valid(const UnitInfo& u, int it, const int* host_len, int ring_S) {
+// Valid keys in the key/value tile of iteration it (<= 0: wholly padding).
+__device__ __forceinline__ int kv_tile_len(const UnitInfo& u, int it, const int* host_len, int ring_S) {
   int kt = u.kt0 - it;  // contiguous ring tiles
   if (u.wrap && kt < 0) kt += u.nkt;
   const int T = ring_S / 128;
   const int j = kt / T, tk = kt - j * T;
-  return tk * 128 < host_len_at(host_len, j, ring_S);
+  return host_len_at(host_len, j, ring_S) - tk * 128;
+}
+__device__ __forceinline__ bool iter_valid(const UnitInfo& u, int it, const int* host_len, int ring_S) {
+  return kv_tile_len(u, it, host_len, ring_S) > 0;
 }
 __device__ __forceinline__ int next_valid(const UnitInfo& u, int it, const int* host_len, int ring_S) {
   ++it;
@@ -500,7 +504,12 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
       }
       bool o_valid = (a.mode == 1);  // O_X holds a state that must be rescaled
       for (int it = ui.striped ? 0 : ui.start[x]; it < ui.n_iter; ++it) {
-        if (!active(ui, x, it) || (VARLEN && !iter_valid(ui, it, a.host_len, a.ring_S))) continue;
+        if (!active(ui, x, it)) continue;
+        int kv_len = 128;  // valid keys of this tile (variable host lengths)
+        if (VARLEN) {
+          kv_len = kv_tile_len(ui, it, a.host_len, a.ring_S);
+          if (kv_len <= 0) continue;
+        }
         if (!mbar_wait(bar_s_full(x), s_cnt & 1, abort_flag, a.status, lim)) { ok = false; break; }
         ++s_cnt;
         tc_fence_after();
@@ -523,13 +532,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
           need_mask = (a.causal && kvpos0 + 127 > ui.qpos0[x]) || (kt * 128 + 128 > a.Nkv);
           lim_c = a.causal ? qpos - kvpos0 : 127;
         }
-        int kv_len = 128;
-        if (VARLEN) {  // keys past the key host's valid length
-          const int T = a.ring_S / 128;
-          const int j = kt / T;
-          kv_len = host_len_at(a.host_len, j, a.ring_S) - (kt - j * T) * 128;
-          if (kv_len < 128) need_mask = true;
-        }
+        if (VARLEN && kv_len < 128) need_mask = true;  // keys past the host's valid length
         if (need_mask) {
           const int nvalid = VARLEN ? min(a.Nkv - kt * 128, kv_len) : a.Nkv - kt * 128;
 #pragma unroll
