@@ -475,8 +475,9 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
           if (qvalid <= 0) { --gi; continue; }
         }
         const int s = gi & 1;
-        const float* lse2 = reinterpret_cast<const float*>(smem + L::kVec0 + s * 1024) + half * 64;
-        const float* dvec = lse2 + 128;
+        // -LSE*log2(e) and -D of this stage's query tile, this half's columns
+        const float* nlse2 = reinterpret_cast<const float*>(smem + L::kVec0 + s * 1024) + half * 64;
+        const float* ndvec = nlse2 + 128;
         if (!mbar_wait(BAR_S_FULL, gi & 1, abort_flag, a.status, lim)) { ok = false; break; }
         // the LSE / D slices of this stage arrived with the Q tile
         if (!mbar_wait(bar_q_full(s), (gi >> 1) & 1, abort_flag, a.status, lim)) { ok = false; break; }
@@ -499,14 +500,19 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
         } else {
           diag = a.causal && qt == bu.jt;
         }
-        // P^T = exp2(S^T * scale*log2e - LSE*log2e)
+        // P^T = exp2(S^T * scale*log2e - LSE*log2e), two columns per fp32x2 FMA
+        const float2 sl2x2 = make_float2(sl2, sl2);
 #pragma unroll
         for (int c = 0; c < 64; c += 4) {
-          const float4 l4 = *reinterpret_cast<const float4*>(lse2 + c);
-          const float lv[4] = {l4.x, l4.y, l4.z, l4.w};
-#pragma unroll
-          for (int u4 = 0; u4 < 4; ++u4)
-            pr[c + u4] = __float_as_uint(ex2_approx(fmaf(__uint_as_float(pr[c + u4]), sl2, -lv[u4])));
+          const float4 l4 = *reinterpret_cast<const float4*>(nlse2 + c);
+          const float2 a01 = __ffma2_rn(make_float2(__uint_as_float(pr[c]), __uint_as_float(pr[c + 1])), sl2x2,
+                                        make_float2(l4.x, l4.y));
+          const float2 a23 = __ffma2_rn(make_float2(__uint_as_float(pr[c + 2]), __uint_as_float(pr[c + 3])), sl2x2,
+                                        make_float2(l4.z, l4.w));
+          pr[c] = __float_as_uint(ex2_approx(a01.x));
+          pr[c + 1] = __float_as_uint(ex2_approx(a01.y));
+          pr[c + 2] = __float_as_uint(ex2_approx(a23.x));
+          pr[c + 3] = __float_as_uint(ex2_approx(a23.y));
         }
         // the masks, only on the tiles that have any: this half's columns below
         // c_lo (causal) or from c_hi on (padded queries), and every column of
@@ -539,9 +545,11 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
           uint32_t pl[PRECISE ? 16 : 1];
 #pragma unroll
           for (int j = 0; j < 32; j += 2) {
-            const float2 dd = *reinterpret_cast<const float2*>(dvec + c + j);
-            const float d0 = __uint_as_float(pr[c + j]) * (__uint_as_float(dp[j]) - dd.x);
-            const float d1 = __uint_as_float(pr[c + j + 1]) * (__uint_as_float(dp[j + 1]) - dd.y);
+            // dS = P * (dP - D), two columns per fp32x2 add and multiply
+            const float2 ndd = *reinterpret_cast<const float2*>(ndvec + c + j);
+            const float2 diff = __fadd2_rn(make_float2(__uint_as_float(dp[j]), __uint_as_float(dp[j + 1])), ndd);
+            const float2 ds = __fmul2_rn(make_float2(__uint_as_float(pr[c + j]), __uint_as_float(pr[c + j + 1])), diff);
+            const float d0 = ds.x, d1 = ds.y;
             pk[j / 2] = pack_half2(d0, d1);
             if (PRECISE) {
               const float2 hi = unpack_half2(pk[j / 2]);

@@ -81,8 +81,9 @@ cudaError_t launch_finalize(const float* o, const float* m, const float* l, void
 cudaError_t launch_to_f16(const void* src, int src_dtype, long long src_bs, void* dst,
                           int B, long long elems_per_batch, int* status,
                           cudaStream_t st);
-// D[b, h, n] = sum_c dO[b, n, h, c] * O[b, n, h, c]; when lse2 is given also
-// lse2[b, h, n] = lse[b, h, n] * log2(e) (the backward kernel's exponent offset).
+// D[b, h, n] = sum_c dO[b, n, h, c] * O[b, n, h, c].  When lse2 is given (the
+// tensor-core backward) both come out negated: D[b, h, n] = -sum(...) and
+// lse2[b, h, n] = -lse[b, h, n] * log2(e), the terms that kernel adds.
 cudaError_t launch_bwd_dot(const void* dO, int do_dtype, const void* o, int o_dtype,
                            long long q_bs, float* D, const float* lse, float* lse2, int B,
                            int N, int H, int d, cudaStream_t st);
@@ -142,8 +143,8 @@ struct TcBwdArgs {
   int ring_P, ring_S;
   int striped;  // causal, rows in striped order (position l*P + host)
   const int* host_len;  // optional: valid rows per host (device, P entries)
-  const float* lse;   // [B, Hq, N], multiplied by log2(e)
-  const float* Dvec;  // [B, Hq, N]
+  const float* lse;   // [B, Hq, N]: -LSE * log2(e)
+  const float* Dvec;  // [B, Hq, N]: -D
   float* dq_acc;      // packed fp32 [B, N, Hq, d], pre-zeroed, reduce-added
   void* dk;           // [B, N, Hkv, d] in grad_dtype, batch stride kv_bs
   void* dv;

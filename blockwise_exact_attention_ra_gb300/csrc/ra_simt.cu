@@ -422,8 +422,12 @@ __global__ void bwd_dot_kernel(const void* dO, int do_dtype, const void* o, int 
   acc = warp_sum(acc);
   if (lane == 0) {
     const long long sidx = ((long long)b * H + h) * N + n;
-    D[sidx] = acc;
-    if (lse2) lse2[sidx] = lse[sidx] * 1.4426950408889634f;
+    if (lse2) {  // tensor-core backward: -D and -LSE*log2(e), added with packed fp32 ops
+      D[sidx] = -acc;
+      lse2[sidx] = -(lse[sidx] * 1.4426950408889634f);
+    } else {
+      D[sidx] = acc;
+    }
   }
 }
 
