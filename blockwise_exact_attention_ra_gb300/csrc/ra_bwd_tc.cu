@@ -67,8 +67,8 @@ struct BwdSmem {
   static constexpr int kBars = kVec0 + 2 * 1024;
   // kv_full, kv_empty, q_full[2], q_empty[2], s_full, dp_full, ds_full,
   // ds_free, dq_full, dq_free, dkv_full, dkv_free, drain, dq_staged,
-  // do_full[2], do_empty[2], dq_drained
-  static constexpr int kNumBars = 21;
+  // do_full[2], do_empty[2], dq_drained, p_full
+  static constexpr int kNumBars = 22;
   static constexpr int kMisc = kBars + kNumBars * 8;
   static constexpr int kUsed = kMisc + 16;
   // at least 120 KB so that one CTA (holding all 512 TMEM columns) occupies an SM
@@ -222,7 +222,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
   auto bar_q_empty = [&](int s) { return bar0 + 32 + 8 * s; };
   auto bar_do_full = [&](int s) { return bar0 + 128 + 8 * s; };
   auto bar_do_empty = [&](int s) { return bar0 + 144 + 8 * s; };
-  const uint32_t BAR_DQ_DRAINED = bar0 + 160;
+  const uint32_t BAR_DQ_DRAINED = bar0 + 160, BAR_P_FULL = bar0 + 168;
   const uint32_t BAR_S_FULL = bar0 + 48, BAR_DP_FULL = bar0 + 56, BAR_DS_FULL = bar0 + 64,
                  BAR_DS_FREE = bar0 + 72, BAR_DQ_FULL = bar0 + 80, BAR_DQ_FREE = bar0 + 88,
                  BAR_DKV_FULL = bar0 + 96, BAR_DKV_FREE = bar0 + 104, BAR_DRAIN = bar0 + 112,
@@ -253,6 +253,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
     mbar_init(BAR_DRAIN, 1);
     mbar_init(BAR_DQ_STAGED, 128);
     mbar_init(BAR_DQ_DRAINED, 1);
+    mbar_init(BAR_P_FULL, 256);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -340,7 +341,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
       // dQ = dS K: A = dS^T viewed MN-major (M = queries), B = K MN-major
       const uint32_t id_dq = idesc_f16(0, 1, 1, 128, D);
       const uint32_t sK = sbase + L::kK, sV = sbase + L::kV, sDS = sbase + L::kDS;
-      uint32_t qd_cnt = 0, ds_cnt = 0, dq_cnt = 0;
+      uint32_t qd_cnt = 0, ds_cnt = 0, dq_cnt = 0, p_cnt = 0;
       int k = 0;
       bool ok = true;
       // descriptors built once: K-major (LBO unused) and MN-major (LBO = the
@@ -386,11 +387,20 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
         mma_nt(T_DP, dV_k, dO_k0 + s * kStageStep);
         mma_commit(BAR_DP_FULL);
         const int it0 = VARLEN ? next_valid(bu, 0) : 0;
+        // Per iteration i, in this order:
+        //   P(i) stored     -> dV(i) += P^T dO_i, then S(i+1) into the same columns
+        //   dS(i) stored    -> dQ(i) = dS K, then dK(i) += dS^T Q_i (dK first with
+        //                      RA_PRECISE: its low terms sit in the dP columns)
+        //   dQ(i) read out  -> dP(i+1) into the dP/dQ columns
+        // so the compute warps form P(i+1) while dQ(i) and dK(i) run, and dP(i+1)
+        // only waits for dQ(i) to leave TMEM.
         for (int it = it0, nx; it < bu.n_iter; it = nx) {
           nx = VARLEN ? next_valid(bu, it + 1) : it + 1;
           const uint64_t dQ_mn = dQ_mn0 + s * kStageStep, dO_mn = dO_mn0 + s * kStageStep;
-          if (!wait(BAR_DS_FULL, ds_cnt & 1)) break;
-          ++ds_cnt;
+          const bool has_next = nx < bu.n_iter;
+          const uint32_t s2 = (qd_cnt + 1) & 1, par2 = ((qd_cnt + 1) >> 1) & 1;
+          if (!wait(BAR_P_FULL, p_cnt & 1)) break;
+          ++p_cnt;
           if (it == it0 && k > 0 && !wait(BAR_DKV_FREE, (k - 1) & 1)) break;
           // dV += P^T dO_i   (P^T in TMEM: queries 0-63 at columns 0-31, 64-127 at 64-95)
 #pragma unroll
@@ -398,13 +408,22 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
             const uint32_t pa = T_S + (kk < 4 ? kk * 8 : 64 + (kk - 4) * 8);
             mma_ts(T_DV, pa, desc_off(dO_mn, kk * 2048), id_acc, (it > it0 || kk > 0) ? 1u : 0u);
           }
-          const bool has_next = nx < bu.n_iter;
-          const uint32_t s2 = (qd_cnt + 1) & 1, par2 = ((qd_cnt + 1) >> 1) & 1;
           if (has_next) {
             if (!wait(bar_q_full(s2), par2)) break;
             mma_nt(T_S, dK_k, dQ_k0 + s2 * kStageStep);
             mma_commit(BAR_S_FULL);
           }
+          if (!wait(BAR_DS_FULL, ds_cnt & 1)) break;
+          ++ds_cnt;
+          // dQ_i = dS K   (the dS^T tile read MN-major: M = queries)
+          auto issue_dq = [&]() {
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk)
+              mma_ss(T_DP, desc_off(dS_mn, kk * 2048), desc_off(dK_mn, kk * 2048), id_dq, kk > 0 ? 1u : 0u);
+            mma_commit(BAR_DQ_FULL);  // dO_i (read by dP_i, dV_i) is consumed too: the dQ warps stage dQ_i in its buffer
+            ++dq_cnt;
+          };
+          if (!PRECISE) issue_dq();
           // dK += dS^T Q_i   (dS^T K-major: key rows of 64-query swizzled halves)
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk) {
@@ -419,13 +438,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
             }
           }
           mma_commit(bar_q_empty(s));  // dK was the last reader of Q_i
-          // dQ_i = dS K   (the same dS^T tile read MN-major: M = queries)
-#pragma unroll
-          for (int kk = 0; kk < 8; ++kk) {
-            mma_ss(T_DP, desc_off(dS_mn, kk * 2048), desc_off(dK_mn, kk * 2048), id_dq, kk > 0 ? 1u : 0u);
-          }
-          mma_commit(BAR_DQ_FULL);  // dO_i is consumed too; the dQ warps stage dQ_i in its buffer
-          ++dq_cnt;
+          if (PRECISE) issue_dq();
           mma_commit(BAR_DS_FREE);
           ++qd_cnt;
           if (has_next) {
@@ -532,6 +545,11 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
           for (int j = 0; j < 32; j += 2) pk[j / 2] = pack_half2(__uint_as_float(pr[c + j]), __uint_as_float(pr[c + j + 1]));
           RA_TMEM_ST16(tS + c / 2, pk);
         }
+        // P^T is in TMEM (and S^T has been read): the MMA warp may start dV
+        // and then overwrite these columns with the next S^T
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(BAR_P_FULL);
         if (!mbar_wait(BAR_DP_FULL, gi & 1, abort_flag, a.status, lim)) { ok = false; break; }
         tc_fence_after();
         // dS^T of the previous iteration must have been consumed by its MMAs
