@@ -146,14 +146,15 @@ int make_map(CUtensorMap* m, const void* base, int is_bf16, int B, int N, int H,
   return RA_OK;
 }
 
-// Packed fp32 [B, N, H, d] tensor: box (32, 1, 128, 1), 128-byte swizzle.
+// Packed fp32 [B, N, H, d] tensor: box (32, 1, 32, 1), 128-byte swizzle (one
+// warp's 32 rows of a 32-column slab).
 int make_map_f32(CUtensorMap* m, void* base, int B, int N, int H, int d) {
   EncodeTiledFn fn;
   int rc = encoder(&fn);
   if (rc) return rc;
   cuuint64_t dims[4] = {(cuuint64_t)d, (cuuint64_t)H, (cuuint64_t)N, (cuuint64_t)B};
   cuuint64_t strides[3] = {(cuuint64_t)d * 4, (cuuint64_t)H * d * 4, (cuuint64_t)N * H * d * 4};
-  cuuint32_t box[4] = {32, 1, 128, 1};
+  cuuint32_t box[4] = {32, 1, 32, 1};
   cuuint32_t estr[4] = {1, 1, 1, 1};
   CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, base, dims, strides, box, estr,
                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,

@@ -66,8 +66,8 @@ struct BwdSmem {
   static constexpr int kVec0 = kDS + kDSBytes;  // per stage: LSE*log2e [128], D [128]
   static constexpr int kBars = kVec0 + 2 * 1024;
   // kv_full, kv_empty, q_full[2], q_empty[2], s_full, dp_full, ds_full,
-  // ds_free, dq_full, dq_free, dkv_full, dkv_free, drain, dq_staged,
-  // do_full[2], do_empty[2], dq_drained, p_full
+  // ds_free, dq_full, dq_free, dkv_full, dkv_free, drain, (unused),
+  // do_full[2], do_empty[2], (unused), p_full
   static constexpr int kNumBars = 22;
   static constexpr int kMisc = kBars + kNumBars * 8;
   static constexpr int kUsed = kMisc + 16;
@@ -222,11 +222,10 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
   auto bar_q_empty = [&](int s) { return bar0 + 32 + 8 * s; };
   auto bar_do_full = [&](int s) { return bar0 + 128 + 8 * s; };
   auto bar_do_empty = [&](int s) { return bar0 + 144 + 8 * s; };
-  const uint32_t BAR_DQ_DRAINED = bar0 + 160, BAR_P_FULL = bar0 + 168;
+  const uint32_t BAR_P_FULL = bar0 + 168;
   const uint32_t BAR_S_FULL = bar0 + 48, BAR_DP_FULL = bar0 + 56, BAR_DS_FULL = bar0 + 64,
                  BAR_DS_FREE = bar0 + 72, BAR_DQ_FULL = bar0 + 80, BAR_DQ_FREE = bar0 + 88,
-                 BAR_DKV_FULL = bar0 + 96, BAR_DKV_FREE = bar0 + 104, BAR_DRAIN = bar0 + 112,
-                 BAR_DQ_STAGED = bar0 + 120;
+                 BAR_DKV_FULL = bar0 + 96, BAR_DKV_FREE = bar0 + 104, BAR_DRAIN = bar0 + 112;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kMisc + 4);
   const uint32_t warp = warp_id();
@@ -240,7 +239,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
       mbar_init(bar_q_full(s), 1);
       mbar_init(bar_q_empty(s), 1);
       mbar_init(bar_do_full(s), 1);
-      mbar_init(bar_do_empty(s), 1);
+      mbar_init(bar_do_empty(s), 4);  // one arrival per dQ warp
     }
     mbar_init(BAR_S_FULL, 1);
     mbar_init(BAR_DP_FULL, 1);
@@ -251,8 +250,6 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
     mbar_init(BAR_DKV_FULL, 1);
     mbar_init(BAR_DKV_FREE, 128);
     mbar_init(BAR_DRAIN, 1);
-    mbar_init(BAR_DQ_STAGED, 128);
-    mbar_init(BAR_DQ_DRAINED, 1);
     mbar_init(BAR_P_FULL, 256);
     *abort_flag = 0;
     fence_barrier_init();
@@ -611,14 +608,12 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
         tc_fence_after();
         const int s = (dq_cnt - 1) & 1;  // the stage that held Q_i, dO_i
         constexpr int HALF = D / 2;           // columns per staging round
-        constexpr int BPR = HALF / 32;        // 16 KB boxes per round
-        // round 0: columns [0, HALF) -> dO buffer; box cc, row r, 16-byte
-        // chunk j at r * 128 + ((j ^ (r & 7)) << 4) (128-byte swizzle)
-        {
-          uint32_t v[HALF];
-#pragma unroll
-          for (int c = 0; c < HALF; c += 32) RA_TMEM_LD32(T_DP + lane_off + c, (v + c));
-          tmem_ld_wait();
+        constexpr int BPR = HALF / 32;        // 32-column slabs per round
+        // Each warp stages and reduce-adds its own 32 rows (no cross-warp
+        // hand-off): slab cc of round rd, row r, 16-byte chunk j at
+        // dq_box(s, cc) + r * 128 + ((j ^ (r & 7)) << 4) (128-byte swizzle,
+        // the tensor map's layout; a 32-row box starts at row 32 * quarter).
+        auto stage = [&](const uint32_t* v) {
 #pragma unroll
           for (int cc = 0; cc < BPR; ++cc) {
             uint8_t* box = smem + dq_box<D>(s, cc) + r * 128;
@@ -627,9 +622,26 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
               *reinterpret_cast<uint4*>(box + ((j ^ (r & 7)) << 4)) =
                   make_uint4(v[32 * cc + 4 * j], v[32 * cc + 4 * j + 1], v[32 * cc + 4 * j + 2], v[32 * cc + 4 * j + 3]);
           }
+          fence_proxy_async_smem();
+          __syncwarp();
+        };
+        auto reduce = [&](int rd) {  // lane 0: this warp's rows of round rd
+#pragma unroll
+          for (int cc = 0; cc < BPR; ++cc)
+            tma_reduce_add_4d(&a.tm_dq, sbase + dq_box<D>(s, cc) + quarter * 32 * 128, rd * HALF + 32 * cc, h,
+                              qt * 128 + (int)quarter * 32, bu.b);
+          bulk_commit();
+        };
+        // round 0: columns [0, HALF) -> the dO_i buffer (dP_i and dV_i, its
+        // readers, completed before dQ_i did)
+        {
+          uint32_t v[HALF];
+#pragma unroll
+          for (int c = 0; c < HALF; c += 32) RA_TMEM_LD32(T_DP + lane_off + c, (v + c));
+          tmem_ld_wait();
+          stage(v);
         }
-        fence_proxy_async_smem();
-        mbar_arrive(BAR_DQ_STAGED);
+        if (lane == 0) reduce(0);
         // round 1's columns stay in registers; the TMEM columns go back to the MMA warp
         uint32_t v1[HALF];
 #pragma unroll
@@ -637,33 +649,12 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
         tmem_ld_wait();
         tc_fence_before();
         mbar_arrive(BAR_DQ_FREE);
-        if (warp == 10 && lane == 0) {
-          if (!mbar_wait(BAR_DQ_STAGED, 0, abort_flag, a.status, lim)) { ok = false; break; }
-#pragma unroll
-          for (int cc = 0; cc < BPR; ++cc)
-            tma_reduce_add_4d(&a.tm_dq, sbase + dq_box<D>(s, cc), 32 * cc, h, qt * 128, bu.b);
-          bulk_commit();
-          bulk_wait_read_all();
-          mbar_arrive(BAR_DQ_DRAINED);
-        }
-        if (!mbar_wait(BAR_DQ_DRAINED, (dq_cnt - 1) & 1, abort_flag, a.status, lim)) { ok = false; break; }
-        // round 1: columns [HALF, D) into the same buffer
-#pragma unroll
-        for (int cc = 0; cc < BPR; ++cc) {
-          uint8_t* box = smem + dq_box<D>(s, cc) + r * 128;
-#pragma unroll
-          for (int j = 0; j < 8; ++j)
-            *reinterpret_cast<uint4*>(box + ((j ^ (r & 7)) << 4)) =
-                make_uint4(v1[32 * cc + 4 * j], v1[32 * cc + 4 * j + 1], v1[32 * cc + 4 * j + 2], v1[32 * cc + 4 * j + 3]);
-        }
-        fence_proxy_async_smem();
-        mbar_arrive(BAR_DQ_STAGED);
-        if (warp == 10 && lane == 0) {
-          if (!mbar_wait(BAR_DQ_STAGED, 1, abort_flag, a.status, lim)) { ok = false; break; }
-#pragma unroll
-          for (int cc = 0; cc < BPR; ++cc)
-            tma_reduce_add_4d(&a.tm_dq, sbase + dq_box<D>(s, cc), HALF + 32 * cc, h, qt * 128, bu.b);
-          bulk_commit();
+        if (lane == 0) bulk_wait_read_all();  // this warp's round-0 rows have left shared memory
+        __syncwarp();
+        // round 1: columns [HALF, D) into the same rows
+        stage(v1);
+        if (lane == 0) {
+          reduce(1);
           bulk_wait_read_all();  // the dO buffer may be refilled once the TMA engine has read it
           mbar_arrive(bar_do_empty(s));
         }
@@ -711,7 +702,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
       tc_fence_before();
       mbar_arrive(BAR_DKV_FREE);
     }
-    if (warp == 10 && lane == 0) bulk_wait_all();  // reductions complete before the CTA exits
+    if (lane == 0) bulk_wait_all();  // this warp's reductions complete before the CTA exits
   }
 
   tc_fence_before();
