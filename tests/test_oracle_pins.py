@@ -380,3 +380,20 @@ def test_varlen_ignores_padding_values_and_zeroes_padded_rows(causal):
     # the valid rows are exactly attention over the packed sequence (brute force)
     Op, Lp = oracle.attention_fwd(q[:, rows], k[:, rows], v[:, rows], causal, 0.7)
     np.testing.assert_allclose(O[:, rows], Op, atol=1e-13)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_varlen_empty_host_drops_out(causal):
+    # host 1 holds no tokens: the result is attention over hosts 0 and 2 alone,
+    # forward and backward, and host 1's rows are all padding
+    P, S = 3, 4
+    q, k, v, do = rand(1, P * S, 2, 3), rand(1, P * S, 2, 3), rand(1, P * S, 2, 3), rand(1, P * S, 2, 3)
+    dq, dk, dv, O, L = oracle.attention_varlen(q, k, v, do, P, [S, 0, S], causal, 0.9)
+    keep = np.r_[0:S, 2 * S:3 * S]
+    gq, gk, gv, Ok, Lk, _ = oracle.attention_bwd(q[:, keep], k[:, keep], v[:, keep], do[:, keep], causal, 0.9)
+    np.testing.assert_allclose(O[:, keep], Ok, atol=1e-13)
+    np.testing.assert_allclose(L[:, :, keep], Lk, atol=1e-13)
+    for g, ref in ((dq, gq), (dk, gk), (dv, gv)):
+        np.testing.assert_allclose(g[:, keep], ref, atol=1e-13)
+        assert (g[:, S:2 * S] == 0).all()
+    assert np.isneginf(L[:, :, S:2 * S]).all()
