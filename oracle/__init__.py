@@ -1,4 +1,5 @@
-"""fp64 CPU oracle for blockwise exact attention (test infrastructure only).
+"""fp64 CPU oracle for blockwise exact attention and the blockwise
+feed-forward layer (test infrastructure only).
 
 Only the test suite, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
 ``bench.py`` may import this package.  The CUDA product path never imports,
@@ -18,4 +19,12 @@ from .attention import (  # noqa: F401
     ring_fwd_blocked_striped,
     striped_positions,
     ring_schedule,
+)
+from .ffn import (  # noqa: F401
+    gelu,
+    gelu_grad,
+    ffn_fwd,
+    ffn_bwd,
+    ffn_blocked,
+    ffn_bwd_blocked,
 )
