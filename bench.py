@@ -371,6 +371,49 @@ def run_ours(args, ws, rank, local):
                              "ms_per_step": rf_ms + rb_ms, "fwd_ms": rf_ms, "bwd_ms": rb_ms,
                              "tflops_on_valid_tokens": (lf + lb) / ((rf_ms + rb_ms) * 1e-3) / 1e12}}
 
+    # blockwise feed-forward layer at the same model width (d_model = Hq * d,
+    # hidden 4 d_model, all B * N tokens, blocks of 16384 tokens): forward and
+    # backward timed separately; algorithmic flops count the layer's products
+    # (2 forward, 4 backward), not the backward's recomputation of h
+    ffn = None
+    if not args.no_ffn:
+        from blockwise_exact_attention_ra_gb300.inputs import make_ffn
+        T, dm = B * N, Hq * d
+        dh, blk = 4 * dm, min(16384, B * N)
+        fx, fw1, fw2, fdy = make_ffn(T, dm, dh, torch.bfloat16, dev, 777 + rank)
+        fy = torch.empty(T, dm, dtype=torch.bfloat16, device=dev)
+        fdx = torch.empty(T, dm, dtype=torch.bfloat16, device=dev)
+        fdw1 = torch.empty(dh, dm, dtype=torch.float32, device=dev)
+        fdw2 = torch.empty(dm, dh, dtype=torch.float32, device=dev)
+        fws = torch.empty(ra.ra_ffn_workspace_bytes(ra.RA_BF16, T, dm, dh, blk, True), dtype=torch.uint8,
+                          device=dev)
+        for _ in range(args.warmup):
+            ra.ra_ffn_fwd(fx, fw1, fw2, blk, fy, fws, stream)
+            ra.ra_ffn_bwd(fx, fw1, fw2, fdy, blk, fdx, fdw1, fdw2, fws, stream)
+        torch.cuda.synchronize(dev)
+        fe = [torch.cuda.Event(enable_timing=True) for _ in range(3 * args.steps)]
+        ra.ra_kernel_timing(1)
+        for s_ in range(args.steps):
+            fe[3 * s_].record(stream)
+            ra.ra_ffn_fwd(fx, fw1, fw2, blk, fy, fws, stream)
+            fe[3 * s_ + 1].record(stream)
+            ra.ra_ffn_bwd(fx, fw1, fw2, fdy, blk, fdx, fdw1, fdw2, fws, stream)
+            fe[3 * s_ + 2].record(stream)
+        torch.cuda.synchronize(dev)
+        gemm_ms, gemm_n = ra.ra_kernel_timing_read(ra.RA_KERNEL_GEMM_TC)
+        ra.ra_kernel_timing(0)
+        ra.ra_sync_status(stream)
+        f_ms = sum(fe[3 * i].elapsed_time(fe[3 * i + 1]) for i in range(args.steps)) / args.steps
+        b_ms = sum(fe[3 * i + 1].elapsed_time(fe[3 * i + 2]) for i in range(args.steps)) / args.steps
+        unit = 2.0 * T * dm * dh   # one of the layer's products
+        ffn = {"shape": {"tokens": T, "d_model": dm, "d_hidden": dh, "block": blk, "dtype": "bf16"},
+               "fwd_ms": f_ms, "bwd_ms": b_ms,
+               "fwd_tflops": 2 * unit / (f_ms * 1e-3) / 1e12, "bwd_tflops": 4 * unit / (b_ms * 1e-3) / 1e12,
+               "bwd_executed_tflops": 5 * unit / (b_ms * 1e-3) / 1e12,
+               "gemm_launches": gemm_n, "gemm_avg_tflops": 7 * args.steps * unit / (gemm_ms * 1e-3) / 1e12,
+               "frac_of_peak_fwd": 2 * unit / (f_ms * 1e-3) / 1e12 / peaks["sustained"]}
+        del fx, fw1, fw2, fdy, fy, fdx, fdw1, fdw2, fws
+
     # end to end through the public C-ABI call with host buffers: every step
     # uploads its q, k, v, dO from pinned host memory and downloads O, LSE, dQ,
     # dK, dV (bf16) to pinned host memory.  Steps alternate between two streams
@@ -438,7 +481,7 @@ def run_ours(args, ws, rank, local):
             "pct_of_peak": value / ws / peaks["sustained"],
             "fwd_ms": fwd_ms, "bwd_ms": bwd_ms,
             "fwd_tflops": fwd_fl / (fwd_ms * 1e-3) / 1e12, "bwd_tflops": bwd_fl / (bwd_ms * 1e-3) / 1e12,
-            "kernels": kern, "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "striped": striped, "varlen": varlen,
+            "kernels": kern, "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "striped": striped, "varlen": varlen, "ffn": ffn,
             "gpu_launches": launches, "clocks": clk,
         }
         print(json.dumps(line), flush=True)
@@ -456,6 +499,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-striped", action="store_true", help="skip the striped-layout measurement")
     ap.add_argument("--no-varlen", action="store_true", help="skip the variable-length measurement")
+    ap.add_argument("--no-ffn", action="store_true", help="skip the blockwise feed-forward measurement")
     ap.add_argument("--cpu-rows", type=int, default=3072)
     ap.add_argument("--ref-rows", type=int, default=1024)
     ap.add_argument("--N", type=int, default=None, help="override N (profiling on a smaller case)")

@@ -20,7 +20,7 @@ __all__ = [
     "ra_acc_init", "ra_block_fwd", "ra_block_fwd_workspace_bytes", "ra_merge", "ra_finalize",
     "ra_ring_fwd", "ra_ring_fwd_workspace_bytes", "ra_ring_bwd", "ra_ring_bwd_workspace_bytes",
     "ra_ring_fwd_noalloc", "ra_ring_fwd_varlen", "ra_ring_bwd_varlen", "ra_ring_step_host",
-    "ra_ring_step_host_workspace_bytes",
+    "ra_ring_step_host_workspace_bytes", "ra_ffn_workspace_bytes", "ra_ffn_fwd", "ra_ffn_bwd",
     "ra_sync_status", "ra_last_error", "ra_launch_count", "ra_selftest_timeout",
     "ra_kernel_timing", "ra_kernel_timing_read",
     "ring_attention_fwd", "ring_attention_bwd", "RA_F32", "RA_BF16", "RA_F16",
@@ -71,6 +71,9 @@ def _load():
         "ra_ring_fwd_varlen": (i, [vp, vp, vp, i, sh, i, vp, i, f, vp, i, vp, vp, sz, vp]),
         "ra_ring_step_host": (i, [vp, vp, vp, vp, i, sh, i, i, f, vp, i, vp, vp, vp, vp, i, vp, sz, vp]),
         "ra_ring_step_host_workspace_bytes": (sz, [i, i, i, sh, i]),
+        "ra_ffn_workspace_bytes": (sz, [i, ctypes.c_longlong, i, i, i, i]),
+        "ra_ffn_fwd": (i, [vp, vp, vp, i, ctypes.c_longlong, i, i, i, vp, i, vp, sz, vp]),
+        "ra_ffn_bwd": (i, [vp, vp, vp, vp, i, ctypes.c_longlong, i, i, i, vp, i, vp, vp, vp, sz, vp]),
         "ra_ring_bwd_varlen": (i, [vp, vp, vp, vp, i, vp, vp, i, sh, i, vp, i, f, vp, vp, vp, i, vp, sz, vp]),
         "ra_ring_bwd": (i, [vp, vp, vp, vp, i, vp, vp, i, sh, i, i, f, vp, vp, vp, i, vp, sz, vp]),
         "ra_ring_bwd_workspace_bytes": (sz, [i, i, sh, i]),
@@ -145,7 +148,7 @@ def shape_of(q, k):
     return RaShape(B, Nq, Nkv, Hq, Hkv, d, _bstride(q), _bstride(k))
 
 
-RA_KERNEL_FWD_TC, RA_KERNEL_BWD_TC, RA_KERNEL_FWD_F32, RA_KERNEL_BWD_F32 = 0, 1, 2, 3
+RA_KERNEL_FWD_TC, RA_KERNEL_BWD_TC, RA_KERNEL_FWD_F32, RA_KERNEL_BWD_F32, RA_KERNEL_GEMM_TC = 0, 1, 2, 3, 4
 
 
 def ra_kernel_timing(enable):
@@ -268,6 +271,60 @@ def ra_ring_step_host(q, k, v, dO, P, causal, scale, o, lse, dq, dk, dv, workspa
                                  _flags(causal, precise, striped), float(scale), _ptr(o), _dt(o),
                                  _ptr(lse), _ptr(dq), _ptr(dk), _ptr(dv), _dt(dq), _ptr(workspace),
                                  ws_bytes, _stream(stream)))
+
+
+def ra_ffn_workspace_bytes(dtype, T, d_model, d_hidden, block, backward):
+    return int(lib.ra_ffn_workspace_bytes(dtype, int(T), int(d_model), int(d_hidden), int(block),
+                                          1 if backward else 0))
+
+
+def _ffn_check(x, w1, w2):
+    if x.dim() != 2 or w1.dim() != 2 or w2.dim() != 2:
+        raise RAError(1, "feed-forward tensors are 2-D: x [T, d_model], w1 [d_hidden, d_model], w2 [d_model, d_hidden]")
+    T, dm = x.shape
+    dh = w1.shape[0]
+    if tuple(w1.shape) != (dh, dm) or tuple(w2.shape) != (dm, dh):
+        raise RAError(1, f"weight shapes {tuple(w1.shape)}, {tuple(w2.shape)} do not match x {tuple(x.shape)}")
+    for t in (x, w1, w2):
+        if not t.is_contiguous():
+            raise RAError(1, "feed-forward tensors must be contiguous")
+    return T, dm, dh
+
+
+def ra_ffn_fwd(x, w1, w2, block, y, workspace, stream=None):
+    """y = GELU(x w1^T) w2^T one block of `block` tokens at a time."""
+    T, dm, dh = _ffn_check(x, w1, w2)
+    _check(lib.ra_ffn_fwd(_ptr(x), _ptr(w1), _ptr(w2), _dt(x), T, dm, dh, int(block), _ptr(y), _dt(y),
+                          _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def ra_ffn_bwd(x, w1, w2, dy, block, dx, dw1, dw2, workspace, stream=None):
+    """Gradients of sum(y * dy): dx, and fp32 dw1, dw2 (overwritten)."""
+    T, dm, dh = _ffn_check(x, w1, w2)
+    _check(lib.ra_ffn_bwd(_ptr(x), _ptr(w1), _ptr(w2), _ptr(dy), _dt(x), T, dm, dh, int(block), _ptr(dx),
+                          _dt(dx), _ptr(dw1), _ptr(dw2), _ptr(workspace),
+                          workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def ffn_fwd(x, w1, w2, block=None, y_dtype=None, stream=None):
+    """Convenience wrapper: allocates y and the workspace."""
+    T, dm, dh = _ffn_check(x, w1, w2)
+    block = T if block is None else block
+    y = torch.empty(T, dm, dtype=y_dtype or x.dtype, device=x.device)
+    ws = _workspace(ra_ffn_workspace_bytes(_dt(x), T, dm, dh, block, False), x.device)
+    ra_ffn_fwd(x, w1, w2, block, y, ws, stream)
+    return y
+
+
+def ffn_bwd(x, w1, w2, dy, block=None, dx_dtype=torch.float32, stream=None):
+    T, dm, dh = _ffn_check(x, w1, w2)
+    block = T if block is None else block
+    dx = torch.empty(T, dm, dtype=dx_dtype, device=x.device)
+    dw1 = torch.empty(dh, dm, dtype=torch.float32, device=x.device)
+    dw2 = torch.empty(dm, dh, dtype=torch.float32, device=x.device)
+    ws = _workspace(ra_ffn_workspace_bytes(_dt(x), T, dm, dh, block, True), x.device)
+    ra_ffn_bwd(x, w1, w2, dy, block, dx, dw1, dw2, ws, stream)
+    return dx, dw1, dw2
 
 
 def ra_ring_bwd_workspace_bytes(dtype, grad_dtype, shape, P):

@@ -11,7 +11,7 @@ CSRC = os.path.join(HERE, "csrc")
 ROOT = os.path.dirname(HERE)
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(HERE, "libra.so")
-SOURCES = ["ra_api.cu", "ra_simt.cu", "ra_fwd_tc.cu", "ra_bwd_tc.cu", "ra_noalloc.cu"]
+SOURCES = ["ra_api.cu", "ra_simt.cu", "ra_fwd_tc.cu", "ra_bwd_tc.cu", "ra_gemm_tc.cu", "ra_noalloc.cu"]
 HEADERS = ["ra_device.cuh", "ra_internal.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",

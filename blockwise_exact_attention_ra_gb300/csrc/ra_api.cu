@@ -163,6 +163,29 @@ int make_map_f32(CUtensorMap* m, void* base, int B, int N, int H, int d) {
   return RA_OK;
 }
 
+}  // namespace
+
+// Row-major 16-bit matrix [rows, cols] with leading dimension ld (elements):
+// dims (cols, rows), box (64, box_rows), 128-byte swizzle.
+int make_map_2d(CUtensorMap* m, const void* base, int is_bf16, long long rows, long long cols,
+                long long ld, int box_rows) {
+  EncodeTiledFn fn;
+  int rc = encoder(&fn);
+  if (rc) return rc;
+  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)ld * 2};
+  cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(m, is_bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
+                  const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(RA_ERR_CUDA, "cuTensorMapEncodeTiled (2-D) failed (%d)", (int)r);
+  return RA_OK;
+}
+
+namespace {
+
 // -------------------------------------------------------------- validation
 size_t dtype_size(int dt) { return dt == RA_F32 ? 4 : 2; }
 bool valid_dtype(int dt) { return dt == RA_F32 || dt == RA_BF16 || dt == RA_F16; }
@@ -721,6 +744,176 @@ int ra_ring_bwd_varlen(const void* q, const void* k, const void* v, const void* 
     return fail(RA_ERR_INVALID_ARG, "host_len must be a non-NULL, 4-byte aligned device array");
   return ring_bwd_impl(q, k, v, o, o_dtype, dO, lse, dtype, shape, P, flags, scale, dq, dk, dv,
                        grad_dtype, workspace, ws_bytes, stream, host_len);
+}
+
+#pragma GCC visibility pop
+}  // extern "C"
+
+// ------------------------------------------------ blockwise feed-forward layer
+namespace ra {
+namespace {
+
+struct FfnShape {
+  long long T;
+  int dm, dh, block;
+};
+
+int check_ffn(ra_dtype dtype, long long T, int d_model, int d_hidden, int block, FfnShape* out) {
+  if (dtype != RA_BF16 && dtype != RA_F16)
+    return fail(RA_ERR_UNSUPPORTED, "the feed-forward path takes bf16 or fp16 operands");
+  if (T < 1 || d_model < 1 || d_hidden < 1 || block < 1)
+    return fail(RA_ERR_INVALID_ARG, "non-positive feed-forward size (T=%lld d_model=%d d_hidden=%d block=%d)", T,
+                d_model, d_hidden, block);
+  if (d_model % 256 || d_hidden % 256)
+    return fail(RA_ERR_UNSUPPORTED, "d_model and d_hidden must be multiples of 256 (got %d, %d)", d_model, d_hidden);
+  if (T % 128 || block % 128)
+    return fail(RA_ERR_UNSUPPORTED, "T and block must be multiples of 128 (got %lld, %d)", T, block);
+  if (T >= (1ll << 31) || d_model > 65536 || d_hidden > 262144)
+    return fail(RA_ERR_INVALID_ARG, "feed-forward size too large");
+  *out = FfnShape{T, d_model, d_hidden, (int)(block < T ? block : T)};
+  return RA_OK;
+}
+
+// per-block 16-bit scratch: hidden activations a, GELU'(h), dH
+struct FfnWs {
+  size_t a, g, dh, total;
+};
+FfnWs ffn_layout(const FfnShape& s, bool bwd) {
+  FfnWs w{};
+  const size_t blk = align256((size_t)s.block * s.dh * 2);
+  w.a = 0;
+  w.g = blk;
+  w.dh = 2 * blk;
+  w.total = bwd ? 3 * blk : blk;
+  return w;
+}
+
+struct GemmPlan {
+  int rc = RA_OK;
+  cudaStream_t st;
+  int bf16;
+  int* status;
+  int sms;
+  // C[M, N] = epi(A B^T); a_rows/b_rows are the row counts of the stored matrices
+  int run(const void* A, long long a_rows, long long a_cols, int a_mn, const void* B, long long b_rows,
+          long long b_cols, int b_mn, int M, int N, int K, int epi, void* c, long long ldc, int c_dtype,
+          void* c2 = nullptr, const void* aux = nullptr) {
+    if (rc) return rc;
+    GemmArgs g;
+    memset(&g, 0, sizeof g);
+    if ((rc = make_map_2d(&g.tm_a, A, bf16, a_rows, a_cols, a_cols, a_mn ? 64 : 128)) ||
+        (rc = make_map_2d(&g.tm_b, B, bf16, b_rows, b_cols, b_cols, b_mn ? 64 : 256)))
+      return rc;
+    g.M = M; g.N = N; g.K = K;
+    g.a_mn = a_mn; g.b_mn = b_mn; g.ab_bf16 = bf16;
+    g.epi = epi; g.c = c; g.ldc = ldc; g.c_dtype = c_dtype; g.c2 = c2; g.aux = aux;
+    g.status = status;
+    g.wait_limit_ns = wait_limit_ns();
+    cudaError_t e;
+    {
+      TimedLaunch tl(RA_KERNEL_GEMM_TC, st);
+      e = launch_tc_gemm(g, sms, st);
+    }
+    if (e != cudaSuccess) rc = cuda_fail(e, "tensor-core GEMM launch");
+    return rc;
+  }
+};
+
+int ffn_common(const void* x, const void* w1, const void* w2, ra_dtype dtype, long long T, int d_model,
+               int d_hidden, int block, void* workspace, size_t ws_bytes, bool bwd, FfnShape* s, FfnWs* w,
+               int** st) {
+  int rc;
+  if ((rc = check_ffn(dtype, T, d_model, d_hidden, block, s))) return rc;
+  if ((rc = check_ptr(x, "x")) || (rc = check_ptr(w1, "w1")) || (rc = check_ptr(w2, "w2"))) return rc;
+  *w = ffn_layout(*s, bwd);
+  if (!workspace || ws_bytes < w->total)
+    return fail(RA_ERR_INVALID_ARG, "workspace of %zu bytes needed (got %zu)", w->total, ws_bytes);
+  if ((rc = check_ptr(workspace, "workspace"))) return rc;
+  if ((rc = status_ptr(st))) return rc;
+  if (!device_is_sm103()) return fail(RA_ERR_UNSUPPORTED, "tensor-core kernels are built for sm_103a only");
+  return RA_OK;
+}
+
+}  // namespace
+}  // namespace ra
+
+extern "C" {
+#pragma GCC visibility push(default)
+
+size_t ra_ffn_workspace_bytes(ra_dtype dtype, long long T, int d_model, int d_hidden, int block, int backward) {
+  FfnShape s;
+  if (check_ffn(dtype, T, d_model, d_hidden, block, &s)) return 0;
+  return ffn_layout(s, backward != 0).total;
+}
+
+int ra_ffn_fwd(const void* x, const void* w1, const void* w2, ra_dtype dtype, long long T, int d_model,
+               int d_hidden, int block, void* y, ra_dtype y_dtype, void* workspace, size_t ws_bytes, void* stream) {
+  FfnShape s;
+  FfnWs w;
+  int* st;
+  int rc = ffn_common(x, w1, w2, dtype, T, d_model, d_hidden, block, workspace, ws_bytes, false, &s, &w, &st);
+  if (rc) return rc;
+  if (!valid_dtype(y_dtype)) return fail(RA_ERR_INVALID_ARG, "bad y dtype");
+  if ((rc = check_ptr(y, "y"))) return rc;
+  GemmPlan g;
+  g.st = static_cast<cudaStream_t>(stream);
+  g.bf16 = dtype == RA_BF16;
+  g.status = st;
+  g.sms = device_sms();
+  char* ws = static_cast<char*>(workspace);
+  const size_t es = 2, ys = dtype_size(y_dtype);
+  for (long long t0 = 0; t0 < s.T && !g.rc; t0 += s.block) {
+    const int Mb = (int)(s.T - t0 < s.block ? s.T - t0 : s.block);
+    const char* xb = static_cast<const char*>(x) + (size_t)t0 * s.dm * es;
+    // a = GELU(x W1^T) for this block of tokens only
+    g.run(xb, Mb, s.dm, 0, w1, s.dh, s.dm, 0, Mb, s.dh, s.dm, GEMM_GELU, ws + w.a, s.dh, dtype);
+    // y = a W2^T
+    g.run(ws + w.a, Mb, s.dh, 0, w2, s.dm, s.dh, 0, Mb, s.dm, s.dh, GEMM_STORE,
+          static_cast<char*>(y) + (size_t)t0 * s.dm * ys, s.dm, y_dtype);
+  }
+  return g.rc;
+}
+
+int ra_ffn_bwd(const void* x, const void* w1, const void* w2, const void* dy, ra_dtype dtype, long long T,
+               int d_model, int d_hidden, int block, void* dx, ra_dtype dx_dtype, float* dw1, float* dw2,
+               void* workspace, size_t ws_bytes, void* stream) {
+  FfnShape s;
+  FfnWs w;
+  int* st;
+  int rc = ffn_common(x, w1, w2, dtype, T, d_model, d_hidden, block, workspace, ws_bytes, true, &s, &w, &st);
+  if (rc) return rc;
+  if (!valid_dtype(dx_dtype)) return fail(RA_ERR_INVALID_ARG, "bad dx dtype");
+  if ((rc = check_ptr(dy, "dy")) || (rc = check_ptr(dx, "dx")) || (rc = check_ptr(dw1, "dw1")) ||
+      (rc = check_ptr(dw2, "dw2")))
+    return rc;
+  GemmPlan g;
+  g.st = static_cast<cudaStream_t>(stream);
+  g.bf16 = dtype == RA_BF16;
+  g.status = st;
+  g.sms = device_sms();
+  char* ws = static_cast<char*>(workspace);
+  const size_t es = 2, xs = dtype_size(dx_dtype);
+  cudaError_t e = cudaMemsetAsync(dw1, 0, (size_t)s.dh * s.dm * 4, g.st);
+  if (e == cudaSuccess) e = cudaMemsetAsync(dw2, 0, (size_t)s.dm * s.dh * 4, g.st);
+  if (e != cudaSuccess) return cuda_fail(e, "zero weight gradients");
+  for (long long t0 = 0; t0 < s.T && !g.rc; t0 += s.block) {
+    const int Mb = (int)(s.T - t0 < s.block ? s.T - t0 : s.block);
+    const char* xb = static_cast<const char*>(x) + (size_t)t0 * s.dm * es;
+    const char* dyb = static_cast<const char*>(dy) + (size_t)t0 * s.dm * es;
+    // recompute the block's hidden activations: a = GELU(h), g = GELU'(h), h = x W1^T
+    g.run(xb, Mb, s.dm, 0, w1, s.dh, s.dm, 0, Mb, s.dh, s.dm, GEMM_GELU2, ws + w.a, s.dh, dtype, ws + w.g);
+    // dH = (dy W2) * GELU'(h)   (W2 [dm, dh] read as a [K, N] matrix: MN-major)
+    g.run(dyb, Mb, s.dm, 0, w2, s.dm, s.dh, 1, Mb, s.dh, s.dm, GEMM_MUL, ws + w.dh, s.dh, dtype, nullptr,
+          ws + w.g);
+    // dx = dH W1   (W1 [dh, dm] as [K, N]: MN-major)
+    g.run(ws + w.dh, Mb, s.dh, 0, w1, s.dh, s.dm, 1, Mb, s.dm, s.dh, GEMM_STORE,
+          static_cast<char*>(dx) + (size_t)t0 * s.dm * xs, s.dm, dx_dtype);
+    // dW2 += dy^T a   (M = d_model, N = d_hidden, K = the block's tokens; both operands MN-major)
+    g.run(dyb, Mb, s.dm, 1, ws + w.a, Mb, s.dh, 1, s.dm, s.dh, Mb, GEMM_ACC, dw2, s.dh, RA_F32);
+    // dW1 += dH^T x   (M = d_hidden, N = d_model)
+    g.run(ws + w.dh, Mb, s.dh, 1, xb, Mb, s.dm, 1, s.dh, s.dm, Mb, GEMM_ACC, dw1, s.dm, RA_F32);
+  }
+  return g.rc;
 }
 
 #pragma GCC visibility pop

@@ -162,4 +162,37 @@ void count_launch(unsigned n = 1);
 // Records `msg` as the calling thread's ra_last_error() message; returns code.
 int set_error(int code, const char* msg);
 
+// Row-major 16-bit matrix [rows, cols], leading dimension ld (elements):
+// tensor map with box (64 columns, box_rows rows), 128-byte swizzle.
+int make_map_2d(CUtensorMap* m, const void* base, int is_bf16, long long rows, long long cols,
+                long long ld, int box_rows);
+
+// ----------------------------------------------------------------- GEMM
+// C[M, N] = epilogue(sum_k A(m, k) B(n, k)) on the tensor cores, 16-bit
+// operands, fp32 accumulation.  A is K-major (a row-major [M, K] matrix) or
+// MN-major (a row-major [K, M] matrix); B likewise with N.  Tiles 128 x 256.
+enum GemmEpi {
+  GEMM_STORE = 0,   // c = acc (c_dtype)
+  GEMM_GELU = 1,    // c = GELU(acc) (16-bit)
+  GEMM_GELU2 = 2,   // c = GELU(acc), c2 = GELU'(acc) (16-bit)
+  GEMM_MUL = 3,     // c = acc * aux (16-bit aux and c)
+  GEMM_ACC = 4,     // c += acc (fp32)
+};
+struct GemmArgs {
+  CUtensorMap tm_a;   // K-major: box (64, 128); MN-major: box (64, 64)
+  CUtensorMap tm_b;   // K-major: box (64, 256); MN-major: box (64, 64)
+  int M, N, K;
+  int a_mn, b_mn;
+  int ab_bf16;        // operand type: bf16 (1) or fp16 (0)
+  int epi;
+  void* c;            // row-major [M, N], leading dimension ldc
+  long long ldc;
+  int c_dtype;        // ra_dtype of c
+  void* c2;           // GEMM_GELU2: second output, same layout and type as c
+  const void* aux;    // GEMM_MUL: row-major [M, N], leading dimension ldc, 16-bit
+  int* status;
+  unsigned long long wait_limit_ns;
+};
+cudaError_t launch_tc_gemm(GemmArgs& a, int num_sms, cudaStream_t st);
+
 }  // namespace ra

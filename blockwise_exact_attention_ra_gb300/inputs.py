@@ -98,3 +98,20 @@ def sample_rows(cid, n_random=512, heads=None, tail=512, seed=None):
     rows = sorted(rows)
     tail_rows = [(0, tail_head, i) for i in range(N - tail, N)] if tail else []
     return rows, tail_rows, tail_head
+
+
+def make_ffn(T, d_model, d_hidden, dtype, device, seed):
+    """Seeded synthetic feed-forward inputs: x, dy ~ N(0, 1); W1 ~ N(0, 1/d_model),
+    W2 ~ N(0, 1/d_hidden) (unit-variance activations through both layers), each
+    drawn in fp32 and rounded to dtype."""
+    g = torch.Generator(device=device).manual_seed(seed)
+
+    def draw(shape, std):
+        return (torch.randn(shape, generator=g, dtype=torch.float32, device=device) * std).to(dtype)
+
+    x = draw((T, d_model), 1.0)
+    w1 = draw((d_hidden, d_model), d_model ** -0.5)
+    w2 = draw((d_model, d_hidden), d_hidden ** -0.5)
+    dy = draw((T, d_model), 1.0)
+    return x, w1, w2, dy
+

@@ -256,6 +256,40 @@ int ra_ring_step_host(const void* q, const void* k, const void* v, const void* d
 size_t ra_ring_step_host_workspace_bytes(ra_dtype dtype, ra_dtype o_dtype,
                                          ra_dtype grad_dtype, ra_shape shape, int P);
 
+/* Blockwise feed-forward layer ("Ring Attention with Blockwise Transformers
+ * for Near-Infinite Context", Abstract: self-attention and the feedforward
+ * network are both computed blockwise).  The layer is the Transformer's
+ * position-wise feedforward
+ *     y = GELU(x W1^T) W2^T,   GELU(u) = u Phi(u)  (exact, erf form),
+ * computed one block of `block` tokens at a time so that only one block's
+ * hidden activations [block, d_hidden] exist at once; the result is the same
+ * as the unblocked layer.
+ *   x, y [T, d_model] row-major (tokens of all batches); W1 [d_hidden, d_model],
+ *   W2 [d_model, d_hidden] (output x input); x, W1, W2 (and dy) in `dtype`
+ *   (RA_BF16 or RA_F16), y in y_dtype; fp32 accumulation on the tensor cores.
+ *   Sizes: d_model and d_hidden multiples of 256, T and block multiples of 128
+ *   (the last block may be shorter); else RA_ERR_UNSUPPORTED.
+ *   workspace: device memory of ra_ffn_workspace_bytes() bytes (backward != 0
+ *   for ra_ffn_bwd), 16-byte aligned; it holds the block's hidden activations.
+ *   Ownership and errors as for ra_ring_fwd. */
+size_t ra_ffn_workspace_bytes(ra_dtype dtype, long long T, int d_model, int d_hidden,
+                              int block, int backward);
+int ra_ffn_fwd(const void* x, const void* w1, const void* w2, ra_dtype dtype, long long T,
+               int d_model, int d_hidden, int block, void* y, ra_dtype y_dtype,
+               void* workspace, size_t ws_bytes, void* stream);
+
+/* Backward of the blockwise feed-forward layer: gradients of L = sum(y * dy).
+ * Each block recomputes its hidden activations h = x W1^T (no activation is
+ * kept from the forward), then
+ *     dH = (dy W2) * GELU'(h),  dx = dH W1,  dW2 += dy^T GELU(h),  dW1 += dH^T x.
+ *   dx [T, d_model] in dx_dtype (fully overwritten); dw1 [d_hidden, d_model] and
+ *   dw2 [d_model, d_hidden] fp32, zeroed by the call and summed over blocks.
+ *   GELU(h), GELU'(h) and dH are rounded to `dtype` before they enter a
+ *   product (they are tensor-core operands). */
+int ra_ffn_bwd(const void* x, const void* w1, const void* w2, const void* dy, ra_dtype dtype,
+               long long T, int d_model, int d_hidden, int block, void* dx, ra_dtype dx_dtype,
+               float* dw1, float* dw2, void* workspace, size_t ws_bytes, void* stream);
+
 /* Synchronise `stream`, then return and clear the device status word
  * (RA_OK, RA_ERR_RANGE or RA_ERR_TIMEOUT), or RA_ERR_CUDA if the stream
  * itself reports an error. */
@@ -278,7 +312,8 @@ typedef enum {
   RA_KERNEL_BWD_TC = 1,   /* tensor-core backward */
   RA_KERNEL_FWD_F32 = 2,  /* fp32 CUDA-core forward */
   RA_KERNEL_BWD_F32 = 3,  /* fp32 CUDA-core backward (both kernels) */
-  RA_KERNEL_COUNT = 4
+  RA_KERNEL_GEMM_TC = 4,  /* tensor-core GEMM of the feed-forward layer (every launch) */
+  RA_KERNEL_COUNT = 5
 } ra_kernel_id;
 int ra_kernel_timing(int enable);
 int ra_kernel_timing_read(int kernel, double* total_ms, unsigned long long* launches);

@@ -111,5 +111,25 @@ def test_host_step_workspace_and_validation(ra):
     assert call(shape=ra.RaShape(2, 1024, 1024, 3, 2, 128, 0, 0)) == 1
 
 
+def test_ffn_validation(ra):
+    lib = ra.lib
+    vp = ctypes.c_void_p(4096)
+    ws = ra.ra_ffn_workspace_bytes(ra.RA_BF16, 1024, 512, 2048, 256, True)
+    assert ws >= 3 * 256 * 2048 * 2
+    assert ra.ra_ffn_workspace_bytes(ra.RA_BF16, 1024, 512, 2048, 256, False) >= 256 * 2048 * 2
+    assert ra.ra_ffn_workspace_bytes(ra.RA_F32, 1024, 512, 2048, 256, False) == 0   # fp32 not taken
+    wsz = ctypes.c_size_t(ws)
+
+    def fwd(*, dtype=ra.RA_BF16, T=1024, dm=512, dh=2048, block=256, x=vp, nbytes=wsz):
+        return lib.ra_ffn_fwd(x, vp, vp, dtype, T, dm, dh, block, vp, ra.RA_F32, vp, nbytes, None)
+    assert fwd(dtype=ra.RA_F32) == 2
+    assert fwd(dm=500) == 2 and fwd(dh=2000) == 2 and fwd(T=1000) == 2 and fwd(block=200) == 2
+    assert fwd(T=0) == 1
+    assert fwd(x=None) == 1 and "x" in ra.ra_last_error()
+    assert fwd(nbytes=ctypes.c_size_t(16)) == 1 and "workspace" in ra.ra_last_error()
+    assert lib.ra_ffn_bwd(vp, vp, vp, None, ra.RA_BF16, 1024, 512, 2048, 256, vp, ra.RA_F32, vp, vp, vp,
+                          wsz, None) != 0
+
+
 def test_launch_counter_is_readable(ra):
     assert isinstance(ra.ra_launch_count(), int) and ra.ra_launch_count() >= 0
