@@ -794,10 +794,20 @@ struct GemmPlan {
   int bf16;
   int* status;
   int sms;
+  // a second problem run in the same launch (same K, majorness and epilogue)
+  struct Second {
+    const void* A;
+    long long a_rows, a_cols;
+    const void* B;
+    long long b_rows, b_cols;
+    int M, N;
+    void* c;
+    long long ldc;
+  };
   // C[M, N] = epi(A B^T); a_rows/b_rows are the row counts of the stored matrices
   int run(const void* A, long long a_rows, long long a_cols, int a_mn, const void* B, long long b_rows,
           long long b_cols, int b_mn, int M, int N, int K, int epi, void* c, long long ldc, int c_dtype,
-          void* c2 = nullptr, const void* aux = nullptr) {
+          void* c2 = nullptr, const void* aux = nullptr, const Second* second = nullptr) {
     if (rc) return rc;
     GemmArgs g;
     memset(&g, 0, sizeof g);
@@ -807,6 +817,16 @@ struct GemmPlan {
     g.M = M; g.N = N; g.K = K;
     g.a_mn = a_mn; g.b_mn = b_mn; g.ab_bf16 = bf16;
     g.epi = epi; g.c = c; g.ldc = ldc; g.c_dtype = c_dtype; g.c2 = c2; g.aux = aux;
+    g.groups = 1;
+    if (second) {
+      g.groups = 2;
+      if ((rc = make_map_2d(&g.tm_a2, second->A, bf16, second->a_rows, second->a_cols, second->a_cols,
+                            a_mn ? 64 : 128)) ||
+          (rc = make_map_2d(&g.tm_b2, second->B, bf16, second->b_rows, second->b_cols, second->b_cols,
+                            b_mn ? 64 : 256)))
+        return rc;
+      g.M2 = second->M; g.N2 = second->N; g.c_g2 = second->c; g.ldc_g2 = second->ldc;
+    }
     g.status = status;
     g.wait_limit_ns = wait_limit_ns();
     cudaError_t e;
@@ -909,9 +929,11 @@ int ra_ffn_bwd(const void* x, const void* w1, const void* w2, const void* dy, ra
     g.run(ws + w.dh, Mb, s.dh, 0, w1, s.dh, s.dm, 1, Mb, s.dm, s.dh, GEMM_STORE,
           static_cast<char*>(dx) + (size_t)t0 * s.dm * xs, s.dm, dx_dtype);
     // dW2 += dy^T a   (M = d_model, N = d_hidden, K = the block's tokens; both operands MN-major)
-    g.run(dyb, Mb, s.dm, 1, ws + w.a, Mb, s.dh, 1, s.dm, s.dh, Mb, GEMM_ACC, dw2, s.dh, RA_F32);
-    // dW1 += dH^T x   (M = d_hidden, N = d_model)
-    g.run(ws + w.dh, Mb, s.dh, 1, xb, Mb, s.dm, 1, s.dh, s.dm, Mb, GEMM_ACC, dw1, s.dm, RA_F32);
+    // and, in the same launch, dW1 += dH^T x   (M = d_hidden, N = d_model): each alone has
+    // too few 128 x 256 tiles to keep the last wave of SMs busy
+    const GemmPlan::Second dw1_prob{ws + w.dh, Mb, s.dh, xb, Mb, s.dm, s.dh, s.dm, dw1, s.dm};
+    g.run(dyb, Mb, s.dm, 1, ws + w.a, Mb, s.dh, 1, s.dm, s.dh, Mb, GEMM_ACC, dw2, s.dh, RA_F32, nullptr, nullptr,
+          &dw1_prob);
   }
   return g.rc;
 }

@@ -91,9 +91,23 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + kMisc + 4);
   const uint32_t warp = warp_id();
   const uint32_t lane = lane_id();
+  // tiles of the first problem, then (grouped launch) of the second
   const int tiles_n = a.N / kBN;
-  const int num_tiles = (a.M / kBM) * tiles_n;
+  const int tiles0 = (a.M / kBM) * tiles_n;
+  const int tiles_n2 = a.groups > 1 ? a.N2 / kBN : 1;
+  const int num_tiles = tiles0 + (a.groups > 1 ? (a.M2 / kBM) * tiles_n2 : 0);
   const int k_steps = a.K / kBK;
+  auto tile_at = [&](int t, int* m0, int* n0) {  // returns the problem index
+    if (t < tiles0) {
+      *m0 = (t / tiles_n) * kBM;
+      *n0 = (t % tiles_n) * kBN;
+      return 0;
+    }
+    t -= tiles0;
+    *m0 = (t / tiles_n2) * kBM;
+    *n0 = (t % tiles_n2) * kBN;
+    return 1;
+  };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -115,6 +129,10 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&a.tm_a);
     tma_prefetch_desc(&a.tm_b);
+    if (a.groups > 1) {
+      tma_prefetch_desc(&a.tm_a2);
+      tma_prefetch_desc(&a.tm_b2);
+    }
   }
   tc_fence_before();
   __syncthreads();
@@ -131,7 +149,10 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
       int issued[kStages] = {0, 0, 0, 0};
       uint32_t last_phase[kStages] = {0, 0, 0, 0};
       for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
-        const int m0 = (t / tiles_n) * kBM, n0 = (t % tiles_n) * kBN;
+        int m0, n0;
+        const int grp = tile_at(t, &m0, &n0);
+        const CUtensorMap* ma = grp ? &a.tm_a2 : &a.tm_a;
+        const CUtensorMap* mb = grp ? &a.tm_b2 : &a.tm_b;
         for (int kb = 0; kb < k_steps; ++kb, ++cnt) {
           const int s = cnt % kStages;
           const uint32_t ph = (cnt / kStages) & 1;
@@ -141,15 +162,15 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
           const int k0 = kb * kBK;
           if (A_MN) {
 #pragma unroll
-            for (int c = 0; c < kBM / 64; ++c) tma_load_2d(dA + c * 8192, &a.tm_a, bar_full(s), m0 + 64 * c, k0, pol);
+            for (int c = 0; c < kBM / 64; ++c) tma_load_2d(dA + c * 8192, ma, bar_full(s), m0 + 64 * c, k0, pol);
           } else {
-            tma_load_2d(dA, &a.tm_a, bar_full(s), k0, m0, pol);
+            tma_load_2d(dA, ma, bar_full(s), k0, m0, pol);
           }
           if (B_MN) {
 #pragma unroll
-            for (int c = 0; c < kBN / 64; ++c) tma_load_2d(dB + c * 8192, &a.tm_b, bar_full(s), n0 + 64 * c, k0, pol);
+            for (int c = 0; c < kBN / 64; ++c) tma_load_2d(dB + c * 8192, mb, bar_full(s), n0 + 64 * c, k0, pol);
           } else {
-            tma_load_2d(dB, &a.tm_b, bar_full(s), k0, n0, pol);
+            tma_load_2d(dB, mb, bar_full(s), k0, n0, pol);
           }
           issued[s] = 1;
           last_phase[s] = ph;
@@ -207,8 +228,12 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
       const uint32_t b = lt & 1;
       if (!mbar_wait(bar_acc_full(b), (lt >> 1) & 1, abort_flag, a.status, lim)) { ok = false; break; }
       tc_fence_after();
-      const long long row = (long long)(t / tiles_n) * kBM + quarter * 32 + lane;
-      const int col0 = (t % tiles_n) * kBN + half * 128;
+      int m0, n0;
+      const int grp = tile_at(t, &m0, &n0);
+      void* cbase = grp ? a.c_g2 : a.c;
+      const long long ldc = grp ? a.ldc_g2 : a.ldc;
+      const long long row = (long long)m0 + quarter * 32 + lane;
+      const int col0 = n0 + half * 128;
       const uint32_t src = tmem + b * kBN + half * 128 + ((quarter * 32) << 16);
 #pragma unroll 1
       for (int c = 0; c < 128; c += 32) {
@@ -218,24 +243,24 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
         float v[32];
 #pragma unroll
         for (int j = 0; j < 32; ++j) v[j] = __uint_as_float(r[j]);
-        const long long off = row * a.ldc + col0 + c;
+        const long long off = row * ldc + col0 + c;
         if (EPI == GEMM_STORE) {
           if (a.c_dtype == RA_F32) {
-            float4* o = reinterpret_cast<float4*>(static_cast<float*>(a.c) + off);
+            float4* o = reinterpret_cast<float4*>(static_cast<float*>(cbase) + off);
 #pragma unroll
             for (int j = 0; j < 8; ++j) o[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
           } else {
-            store16x32(static_cast<uint16_t*>(a.c) + off, v, a.c_dtype == RA_BF16);
+            store16x32(static_cast<uint16_t*>(cbase) + off, v, a.c_dtype == RA_BF16);
           }
         } else if (EPI == GEMM_GELU) {
 #pragma unroll
           for (int j = 0; j < 32; ++j) v[j] = gelu_f(v[j], nullptr);
-          store16x32(static_cast<uint16_t*>(a.c) + off, v, bf16);
+          store16x32(static_cast<uint16_t*>(cbase) + off, v, bf16);
         } else if (EPI == GEMM_GELU2) {
           float g[32];
 #pragma unroll
           for (int j = 0; j < 32; ++j) v[j] = gelu_f(v[j], &g[j]);
-          store16x32(static_cast<uint16_t*>(a.c) + off, v, bf16);
+          store16x32(static_cast<uint16_t*>(cbase) + off, v, bf16);
           store16x32(static_cast<uint16_t*>(a.c2) + off, g, bf16);
         } else if (EPI == GEMM_MUL) {
           const uint4* m = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(a.aux) + off);
@@ -250,9 +275,9 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
               v[8 * j + 2 * q + 1] *= f.y;
             }
           }
-          store16x32(static_cast<uint16_t*>(a.c) + off, v, bf16);
+          store16x32(static_cast<uint16_t*>(cbase) + off, v, bf16);
         } else {  // GEMM_ACC
-          float4* o = reinterpret_cast<float4*>(static_cast<float*>(a.c) + off);
+          float4* o = reinterpret_cast<float4*>(static_cast<float*>(cbase) + off);
 #pragma unroll
           for (int j = 0; j < 8; ++j) {
             float4 x = o[j];
@@ -279,7 +304,10 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
 
 cudaError_t launch_tc_gemm(GemmArgs& a, int num_sms, cudaStream_t st) {
   if (a.M % kBM || a.N % kBN || a.K % kBK || a.M <= 0 || a.N <= 0 || a.K <= 0) return cudaErrorInvalidValue;
-  const int tiles = (a.M / kBM) * (a.N / kBN);
+  if (a.groups < 1) a.groups = 1;
+  if (a.groups > 2 || (a.groups == 2 && (a.M2 % kBM || a.N2 % kBN || a.M2 <= 0 || a.N2 <= 0)))
+    return cudaErrorInvalidValue;
+  const int tiles = (a.M / kBM) * (a.N / kBN) + (a.groups == 2 ? (a.M2 / kBM) * (a.N2 / kBN) : 0);
   const int grid = tiles < num_sms ? tiles : num_sms;
   auto run = [&](auto kernel) {
     cudaError_t err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kAlloc);

@@ -190,6 +190,13 @@ struct GemmArgs {
   int c_dtype;        // ra_dtype of c
   void* c2;           // GEMM_GELU2: second output, same layout and type as c
   const void* aux;    // GEMM_MUL: row-major [M, N], leading dimension ldc, 16-bit
+  // optional second problem of the same kind in the same launch (same K,
+  // operand types and epilogue): its tiles follow the first problem's
+  int groups;         // 1 or 2
+  CUtensorMap tm_a2, tm_b2;
+  int M2, N2;
+  void* c_g2;
+  long long ldc_g2;
   int* status;
   unsigned long long wait_limit_ns;
 };
