@@ -112,7 +112,7 @@ def _sum_identities(dk, dv, do, group, dtype):
                 f"sum_j dV_j - sum_i dO_i (head {g}): max {(sv - dos).abs().max().item():.3e}"
 
 
-def test_config1_fp32_full(ra):
+def test_fp32_noncausal_N512_full(ra):
     from blockwise_exact_attention_ra_gb300.inputs import CONFIGS, make_config
     c = CONFIGS[1]
     q, k, v, do = make_config(1, "cuda")
@@ -123,10 +123,10 @@ def test_config1_fp32_full(ra):
     rq, rk, rv, rO, rL, _ = oracle.attention_bwd(f64(q), f64(k), f64(v), f64(do), c["causal"], scale)
     for name, got, want, kind in (("O", o, rO, "out"), ("LSE", lse, rL, "lse"), ("dQ", dq, rq, "out"),
                                   ("dK", dk, rk, "out"), ("dV", dv, rv, "out")):
-        check(f"config 1 {name}", f64(got), want, torch.float32, kind)
+        check(f"{c['name']} {name}", f64(got), want, torch.float32, kind)
 
 
-def test_config2_forward_rows(ra):
+def test_bf16_causal_N32768_forward_rows(ra):
     from blockwise_exact_attention_ra_gb300.inputs import CONFIGS, make_config, sample_rows
     c = CONFIGS[2]
     q, k, v, _ = make_config(2, "cuda")
@@ -135,8 +135,8 @@ def test_config2_forward_rows(ra):
     ra.ra_sync_status()
     rows, _, _ = sample_rows(2, n_random=1000, tail=0)
     order, r, _ = _oracle_rows(q, k, v, None, rows, True, scale, 1, False)
-    check("config 2 O rows", _gpu_rows(o, order), r["O"], torch.bfloat16)
-    check("config 2 LSE rows", _gpu_lse_rows(lse, order), r["LSE"], torch.bfloat16, "lse")
+    check(f"{c['name']} O rows", _gpu_rows(o, order), r["O"], torch.bfloat16)
+    check(f"{c['name']} LSE rows", _gpu_lse_rows(lse, order), r["LSE"], torch.bfloat16, "lse")
     del q, k, v, o, lse
     _free()
 
@@ -153,29 +153,29 @@ def _fwd_bwd_config(ra, cid, heads, precise, n_random, tail):
     _sum_identities(dk, dv, do, group, c["dtype"])
     rows, tail_rows, tail_head = sample_rows(cid, n_random=n_random, heads=heads, tail=tail)
     order, r, _ = _oracle_rows(q, k, v, do, rows, True, scale, group, False)
-    check(f"config {cid} O rows", _gpu_rows(o, order), r["O"], c["dtype"])
-    check(f"config {cid} LSE rows", _gpu_lse_rows(lse, order), r["LSE"], c["dtype"], "lse")
-    check(f"config {cid} dQ rows", _gpu_rows(dq, order), r["dQ"], c["dtype"])
+    check(f"{c['name']} O rows", _gpu_rows(o, order), r["O"], c["dtype"])
+    check(f"{c['name']} LSE rows", _gpu_lse_rows(lse, order), r["LSE"], c["dtype"], "lse")
+    check(f"{c['name']} dQ rows", _gpu_rows(dq, order), r["dQ"], c["dtype"])
     # the last `tail` keys of the tail head's key/value head: every query head of its group
     g = tail_head // group
     N = c["N"]
     trows = [(0, h, i) for h in range(g * group, (g + 1) * group) for i in range(N - tail, N)]
     order_t, rt, kvg = _oracle_rows(q, k, v, do, trows, True, scale, group, True)
-    check(f"config {cid} tail dQ", _gpu_rows(dq, order_t), rt["dQ"], c["dtype"])
-    check(f"config {cid} tail dK", f64(dk[0, N - tail:, g]), kvg[g][0][N - tail:], c["dtype"])
-    check(f"config {cid} tail dV", f64(dv[0, N - tail:, g]), kvg[g][1][N - tail:], c["dtype"])
+    check(f"{c['name']} tail dQ", _gpu_rows(dq, order_t), rt["dQ"], c["dtype"])
+    check(f"{c['name']} tail dK", f64(dk[0, N - tail:, g]), kvg[g][0][N - tail:], c["dtype"])
+    check(f"{c['name']} tail dV", f64(dv[0, N - tail:, g]), kvg[g][1][N - tail:], c["dtype"])
     del q, k, v, do, o, lse, dq, dk, dv
     _free()
 
 
-def test_config3_fwd_bwd(ra):
+def test_bf16_causal_N131072_fwd_bwd(ra):
     _fwd_bwd_config(ra, 3, heads=[1, 6, 11, 15], precise=False, n_random=512, tail=512)
 
 
-def test_config4_gqa_stress_fwd_bwd(ra):
+def test_bf16_gqa_stress_N262144_fwd_bwd(ra):
     # logits up to ~+-30 and +-50 outliers in V: two-term fp16 products
     _fwd_bwd_config(ra, 4, heads=[0, 1, 2, 3, 20, 21, 22, 23], precise=True, n_random=512, tail=256)
 
 
-def test_config5_one_million_tokens(ra):
+def test_bf16_causal_N1048576_fwd_bwd(ra):
     _fwd_bwd_config(ra, 5, heads=[3, 29], precise=False, n_random=512, tail=256)
