@@ -131,5 +131,27 @@ def test_ffn_validation(ra):
                           wsz, None) != 0
 
 
+def test_rejected_flag_combinations(ra):
+    lib = ra.lib
+    sh = ra.RaShape(1, 1024, 1024, 2, 2, 128, 0, 0)
+    vp = ctypes.c_void_p(4096)
+    hl = ctypes.c_void_p(8192)
+    both = ra.RA_CAUSAL | ra.RA_STRIPED
+    # the striped layout and per-host lengths do not combine
+    assert lib.ra_ring_fwd_varlen(vp, vp, vp, ra.RA_BF16, sh, 4, hl, both, 0.1, vp, ra.RA_F32, vp, vp,
+                                  ctypes.c_size_t(1 << 30), None) == 1
+    assert "STRIPED" in ra.ra_last_error()
+    assert lib.ra_ring_bwd_varlen(vp, vp, vp, vp, ra.RA_F32, vp, vp, ra.RA_BF16, sh, 4, hl, both, 0.1, vp, vp, vp,
+                                  ra.RA_F32, vp, ctypes.c_size_t(1 << 30), None) == 1
+    # a missing or misaligned length array
+    assert lib.ra_ring_fwd_varlen(vp, vp, vp, ra.RA_BF16, sh, 4, None, 1, 0.1, vp, ra.RA_F32, vp, vp,
+                                  ctypes.c_size_t(1 << 30), None) == 1
+    assert lib.ra_ring_fwd_varlen(vp, vp, vp, ra.RA_BF16, sh, 4, ctypes.c_void_p(8194), 1, 0.1, vp, ra.RA_F32,
+                                  vp, vp, ctypes.c_size_t(1 << 30), None) == 1
+    # unknown flag bits
+    assert lib.ra_ring_fwd(vp, vp, vp, ra.RA_BF16, sh, 4, 64, 0.1, vp, ra.RA_F32, vp, vp, ctypes.c_size_t(1 << 30),
+                           None) == 1
+
+
 def test_launch_counter_is_readable(ra):
     assert isinstance(ra.ra_launch_count(), int) and ra.ra_launch_count() >= 0
