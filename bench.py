@@ -252,7 +252,9 @@ def run_reference(args, ws, rank):
                    "d": W["d"], "P": W["P"], "causal": True, "parallelism": "replicas"},
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
                          "sample": f"{args.ref_rows} seeded query rows of one head per step, fwd+bwd "
-                                   f"(incl. their dK/dV contributions), fp64 numpy"},
+                                   f"(incl. their dK/dV contributions), fp64 numpy",
+                         "extrapolated_full_step_s": sum(algo_flops(W["B"], W["N"], W["Hq"], W["d"])) / (value * 1e12),
+                         "extrapolation": "the workload's algorithmic flops at the sampled rows' rate"},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -513,6 +515,8 @@ def run_ours(args, ws, rank, local):
         rows = sample_rows(N, Hq, args.cpu_rows, 4242)
         dt, fl = cpu_oracle_sample(q, k, v, do, rows, True, scale)
         cpu = {"value": fl / dt / 1e12, "unit": "TFLOP/s", "cores": oracle_threads(), "kind": "oracle",
+               "extrapolated_full_step_s": (fwd_fl + bwd_fl) / (fl / dt),
+               "extrapolation": "the workload's algorithmic flops at the sampled rows' rate",
                "sample": f"{args.cpu_rows} seeded query rows of one head, fwd+bwd incl. their dK/dV "
                          f"contributions, fp64 numpy; {dt:.1f} s"}
 
