@@ -539,25 +539,39 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
           for (int c = 0; c < 128; ++c)
             if (c > lim_c || c >= nvalid) sr[c] = __float_as_uint(-INFINITY);
         }
-        float mx = __uint_as_float(sr[0]);
+        // row maximum as eight independent chains of three-input maxima, so
+        // the exponentials can start after ~10 dependent steps instead of 127
+        float mk[8];
 #pragma unroll
-        for (int c = 1; c < 128; ++c) mx = fmaxf(mx, __uint_as_float(sr[c]));
+        for (int k = 0; k < 8; ++k)
+          mk[k] = fmax3(__uint_as_float(sr[k]), __uint_as_float(sr[k + 8]), __uint_as_float(sr[k + 16]));
+#pragma unroll
+        for (int c = 24; c < 120; c += 16) {
+#pragma unroll
+          for (int k = 0; k < 8; ++k)
+            mk[k] = fmax3(mk[k], __uint_as_float(sr[c + k]), __uint_as_float(sr[c + 8 + k]));
+        }
+#pragma unroll
+        for (int k = 0; k < 8; ++k) mk[k] = fmaxf(mk[k], __uint_as_float(sr[120 + k]));
+        const float mx = fmax3(fmax3(mk[0], mk[1], mk[2]), fmax3(mk[3], mk[4], mk[5]), fmaxf(mk[6], mk[7]));
         const float m_tile = mx * sl2;  // -inf stays -inf (scale > 0)
         float m_use = m_run;
         if (m_tile > m_run + kRescaleThreshold) m_use = m_tile;  // also when m_run = -inf
         const bool rescale = (m_use != m_run);
         const float alpha = rescale ? ex2_approx(m_run - m_use) : 1.f;  // exp2(-inf) = 0
         const float neg_m = (m_use == -INFINITY) ? 0.f : -m_use;
-        float rs = 0.f;
+        const float2 sl2x2 = make_float2(sl2, sl2), nm2 = make_float2(neg_m, neg_m);
+        float2 rs2[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
 #pragma unroll
         for (int c = 0; c < 128; c += 32) {
           uint32_t pk[16];
           uint32_t pl[PRECISE ? 16 : 1];
 #pragma unroll
           for (int j = 0; j < 32; j += 2) {
-            const float p0 = ex2_approx(fmaf(__uint_as_float(sr[c + j]), sl2, neg_m));
-            const float p1 = ex2_approx(fmaf(__uint_as_float(sr[c + j + 1]), sl2, neg_m));
-            rs += p0 + p1;
+            const float2 e = __ffma2_rn(make_float2(__uint_as_float(sr[c + j]), __uint_as_float(sr[c + j + 1])),
+                                        sl2x2, nm2);
+            const float p0 = ex2_approx(e.x), p1 = ex2_approx(e.y);
+            rs2[(j / 2) & 1] = __fadd2_rn(rs2[(j / 2) & 1], make_float2(p0, p1));
             pk[j / 2] = pack_half2(p0, p1);
             if (PRECISE) {
               const float2 hi = unpack_half2(pk[j / 2]);
@@ -567,6 +581,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
           RA_TMEM_ST16(tS + c / 2, pk);
           if (PRECISE) RA_TMEM_ST16(tS + 64 + c / 2, pl);
         }
+        const float rs = (rs2[0].x + rs2[1].x) + (rs2[0].y + rs2[1].y);
         l_run = l_run * alpha + rs;
         m_run = m_use;
         if (o_valid && __any_sync(0xffffffffu, rescale)) {
