@@ -469,7 +469,7 @@ int ra_block_fwd(const void* q, const void* k_blk, const void* v_blk, ra_dtype d
   a.B = s.B; a.Nq = s.Nq; a.Nkv = s.Nkv; a.Hq = s.Hq; a.Hkv = s.Hkv; a.d = s.d;
   a.scale_log2 = scale * 1.4426950408889634f;
   a.causal = causal; a.q_off = q_off; a.kv_off = kv_off; a.precise = precise;
-  a.ring_P = 0; a.ring_S = 0; a.mode = 1;
+  a.ring_P = 0; a.ring_S = 0; a.T_m = 0; a.mode = 1;
   a.o_acc = o_acc; a.m_acc = m_acc; a.l_acc = l_acc;
   a.status = st;
   a.wait_limit_ns = wait_limit_ns();
@@ -556,7 +556,7 @@ static int ring_fwd_impl(const void* q, const void* k, const void* v, ra_dtype d
   a.B = s.B; a.Nq = s.Nq; a.Nkv = s.Nkv; a.Hq = s.Hq; a.Hkv = s.Hkv; a.d = s.d;
   a.scale_log2 = scale * 1.4426950408889634f;
   a.causal = causal;
-  a.ring_P = P; a.ring_S = s.Nq / P; a.mode = 0; a.precise = precise; a.striped = striped;
+  a.ring_P = P; a.ring_S = s.Nq / P; a.T_m = div_magic((unsigned)(a.ring_S / 128)); a.mode = 0; a.precise = precise; a.striped = striped;
   a.host_len = host_len;
   if (host_len) {  // padded rows: O = 0, LSE = -inf (the kernel skips them)
     cudaError_t fe = launch_fill_padding(o, o_dtype, s.q_bs, s.B, s.Nq, s.Hq, s.d, P, host_len, lse, cs);
@@ -690,7 +690,7 @@ static int ring_bwd_impl(const void* q, const void* k, const void* v, const void
   a.scale = scale;
   a.scale_log2 = scale * 1.4426950408889634f;
   a.causal = causal;
-  a.ring_P = P; a.ring_S = s.Nq / P; a.precise = precise; a.striped = striped;
+  a.ring_P = P; a.ring_S = s.Nq / P; a.T_m = div_magic((unsigned)(a.ring_S / 128)); a.precise = precise; a.striped = striped;
   a.host_len = host_len;
   if (host_len) {  // padded key rows: dK = dV = 0 (the kernel skips wholly padded key tiles)
     cudaError_t fe = launch_fill_padding(dk, grad_dtype, s.kv_bs, s.B, s.Nkv, s.Hkv, s.d, P, host_len, nullptr, cs);

@@ -80,6 +80,7 @@ struct BwdUnit {
   int count;  // query tiles per head
   int n_iter; // count * group
   int host, tk, per_block;  // striped layouts: key host, local key tile, query tiles per block
+  unsigned long long count_m, pb_m;  // div_magic(count), div_magic(per_block)
 };
 
 // Units are ordered head-major: every resident CTA works on the same
@@ -119,15 +120,18 @@ __device__ __forceinline__ BwdUnit bwd_unit(const TcBwdArgs& a, int u) {
     r.per_block = T - r.tk;
     r.count = a.ring_P * r.per_block;
     r.n_iter = r.count * (a.Hq / a.Hkv);
+    r.count_m = div_magic((unsigned)r.count);
+    r.pb_m = div_magic((unsigned)r.per_block);
     return r;
   }
   r.count = a.causal ? nT - r.jt : nT;
   r.n_iter = r.count * (a.Hq / a.Hkv);
+  r.count_m = div_magic((unsigned)r.count);
   if (VARLEN) {
     // key tiles wholly in their host's padding do no work (their dK, dV rows
     // were zero-filled beforehand)
     const int T = a.ring_S / 128;
-    const int j = r.jt / T;
+    const int j = div_by(r.jt, a.T_m);
     if ((r.jt - j * T) * 128 >= host_len_at(a.host_len, j, a.ring_S)) r.n_iter = 0;
   }
   return r;
@@ -138,11 +142,12 @@ template <bool STRIPED>
 __device__ __forceinline__ void bwd_iter(const TcBwdArgs& a, const BwdUnit& u, int it, int* h,
                                          int* qt) {
   const int group = a.Hq / a.Hkv;
-  const int hh = it / u.count, k = it % u.count;
+  const int hh = div_by(it, u.count_m), k = it - hh * u.count;
   *h = u.g * group + hh;
   if (STRIPED) {  // query hosts (j + s) mod P, local tiles tk..T-1 in each
-    const int s = k / u.per_block;
-    const int qh = (u.host + s) % a.ring_P;
+    const int s = div_by(k, u.pb_m);
+    int qh = u.host + s;  // both < P
+    if (qh >= a.ring_P) qh -= a.ring_P;
     *qt = qh * (a.ring_S / 128) + u.tk + (k - s * u.per_block);
     return;
   }
@@ -151,8 +156,9 @@ __device__ __forceinline__ void bwd_iter(const TcBwdArgs& a, const BwdUnit& u, i
   } else {
     const int nT = a.N / 128;
     const int T = a.ring_S / 128;
-    const int hj = u.jt / T;
-    *qt = (hj * T + k) % nT;
+    int q = div_by(u.jt, a.T_m) * T + k;  // < 2 nT
+    if (q >= nT) q -= nT;
+    *qt = q;
   }
 }
 
@@ -166,7 +172,7 @@ template <bool VARLEN>
 __device__ __forceinline__ bool q_tile_valid(const TcBwdArgs& a, int qt) {
   if (!VARLEN) return true;
   const int T = a.ring_S / 128;
-  const int i = qt / T;
+  const int i = div_by(qt, a.T_m);
   return (qt - i * T) * 128 < host_len_at(a.host_len, i, a.ring_S);
 }
 
@@ -471,7 +477,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
       int kvalid = 128;
       if (VARLEN) {
         const int T = a.ring_S / 128;
-        kvalid = host_len_at(a.host_len, bu.jt / T, a.ring_S) - (bu.jt % T) * 128;
+        const int j = div_by(bu.jt, a.T_m);
+        kvalid = host_len_at(a.host_len, j, a.ring_S) - (bu.jt - j * T) * 128;
       }
       for (int it = 0; it < bu.n_iter; ++it, ++gi) {
         int h, qt;
@@ -481,7 +488,8 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
         int qvalid = 128;
         if (VARLEN) {
           const int T = a.ring_S / 128;
-          qvalid = host_len_at(a.host_len, qt / T, a.ring_S) - (qt % T) * 128;
+          const int i = div_by(qt, a.T_m);
+          qvalid = host_len_at(a.host_len, i, a.ring_S) - (qt - i * T) * 128;
           if (qvalid <= 0) { --gi; continue; }
         }
         const int s = gi & 1;
@@ -505,8 +513,9 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
         int strict = 0;
         if (STRIPED) {
           const int T_local = a.ring_S / 128;
-          diag = qt % T_local == bu.tk;
-          strict = bu.host > qt / T_local ? 1 : 0;
+          const int qhost = div_by(qt, a.T_m);
+          diag = qt - qhost * T_local == bu.tk;
+          strict = bu.host > qhost ? 1 : 0;
         } else {
           diag = a.causal && qt == bu.jt;
         }

@@ -82,6 +82,7 @@ struct UnitInfo {
   // striped causal ring: host `host` visits blocks (host - s) mod P, and in
   // each block the local tiles lead, lead-1, ..., 0 (L = lead + 1 per block)
   int striped, host, P, T, L, tq[2];
+  unsigned long long L_m;  // div_magic(L)
 };
 
 __device__ __forceinline__ int host_len_at(const int* hl, int j, int S) {
@@ -93,7 +94,7 @@ __device__ __forceinline__ int host_len_at(const int* hl, int j, int S) {
 // local tile tk and the block j it belongs to.
 __device__ __forceinline__ int kt_at(const UnitInfo& u, int it, int* tk = nullptr, int* blk = nullptr) {
   if (u.striped) {
-    const int s = it / u.L;
+    const int s = div_by(it, u.L_m);
     const int t = u.kt0 - (it - s * u.L);
     int j = u.host - s;
     if (j < 0) j += u.P;
@@ -109,19 +110,19 @@ __device__ __forceinline__ int kt_at(const UnitInfo& u, int it, int* tk = nullpt
 // With variable host lengths a key/value tile wholly in a host's padding is
 // skipped by every role.
 // Valid keys in the key/value tile of iteration it (<= 0: wholly padding).
-__device__ __forceinline__ int kv_tile_len(const UnitInfo& u, int it, const int* host_len, int ring_S) {
+__device__ __forceinline__ int kv_tile_len(const UnitInfo& u, int it, const TcFwdArgs& a) {
   int kt = u.kt0 - it;  // contiguous ring tiles
   if (u.wrap && kt < 0) kt += u.nkt;
-  const int T = ring_S / 128;
-  const int j = kt / T, tk = kt - j * T;
-  return host_len_at(host_len, j, ring_S) - tk * 128;
+  const int T = a.ring_S / 128;
+  const int j = div_by(kt, a.T_m), tk = kt - j * T;
+  return host_len_at(a.host_len, j, a.ring_S) - tk * 128;
 }
-__device__ __forceinline__ bool iter_valid(const UnitInfo& u, int it, const int* host_len, int ring_S) {
-  return kv_tile_len(u, it, host_len, ring_S) > 0;
+__device__ __forceinline__ bool iter_valid(const UnitInfo& u, int it, const TcFwdArgs& a) {
+  return kv_tile_len(u, it, a) > 0;
 }
-__device__ __forceinline__ int next_valid(const UnitInfo& u, int it, const int* host_len, int ring_S) {
+__device__ __forceinline__ int next_valid(const UnitInfo& u, int it, const TcFwdArgs& a) {
   ++it;
-  while (it < u.n_iter && !iter_valid(u, it, host_len, ring_S)) ++it;
+  while (it < u.n_iter && !iter_valid(u, it, a)) ++it;
   return it;
 }
 
@@ -129,7 +130,7 @@ __device__ __forceinline__ int next_valid(const UnitInfo& u, int it, const int* 
 __device__ __forceinline__ bool active(const UnitInfo& u, int x, int it) {
   if (u.striped) {
     if (x == 1) return u.has_b;
-    return u.kt0 - it % u.L <= u.tq[0];
+    return u.kt0 - (it - div_by(it, u.L_m) * u.L) <= u.tq[0];
   }
   return it >= u.start[x];
 }
@@ -192,6 +193,7 @@ __device__ __forceinline__ UnitInfo unit_info(const TcFwdArgs& a, int u) {
     r.tq[1] = 2 * lp + 1;
     r.kt0 = r.has_b ? r.tq[1] : r.tq[0];  // lead local tile
     r.L = r.kt0 + 1;
+    r.L_m = div_magic((unsigned)r.L);
     r.n_iter = a.ring_P * r.L;
     r.wrap = 0;
     r.start[0] = r.start[1] = 0;
@@ -344,7 +346,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
                         ui.qa_row0 + 128, ui.b, pol_q);
         }
         for (int it = 0; it < ui.n_iter && ok; ++it) {
-          if (VARLEN && !iter_valid(ui, it, a.host_len, a.ring_S)) continue;
+          if (VARLEN && !iter_valid(ui, it, a)) continue;
           int tk = 0, blk = 0;
           const int kt = kt_at(ui, it, &tk, &blk);
 #pragma unroll
@@ -415,7 +417,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
         ++k;
         tc_fence_after();
         // prologue: S of the first valid iteration
-        const int it0 = !VARLEN || iter_valid(ui, 0, a.host_len, a.ring_S) ? 0 : next_valid(ui, 0, a.host_len, a.ring_S);
+        const int it0 = !VARLEN || iter_valid(ui, 0, a) ? 0 : next_valid(ui, 0, a);
         uint32_t sk = L_cnt % kStages;
         if (!mbar_wait(bar_kv_full(sk), (L_cnt / kStages) & 1, abort_flag, a.status, lim)) { ok = false; break; }
         tc_fence_after();
@@ -425,7 +427,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
         ++L_cnt;
         bool first_pv[2] = {a.mode == 0, a.mode == 0};
         for (int it = it0, nx; it < ui.n_iter; it = nx) {
-          nx = VARLEN ? next_valid(ui, it, a.host_len, a.ring_S) : it + 1;
+          nx = VARLEN ? next_valid(ui, it, a) : it + 1;
           const uint32_t sv = L_cnt % kStages;
           if (!mbar_wait(bar_kv_full(sv), (L_cnt / kStages) & 1, abort_flag, a.status, lim)) { ok = false; break; }
           ++L_cnt;
@@ -507,7 +509,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
         if (!active(ui, x, it)) continue;
         int kv_len = 128;  // valid keys of this tile (variable host lengths)
         if (VARLEN) {
-          kv_len = kv_tile_len(ui, it, a.host_len, a.ring_S);
+          kv_len = kv_tile_len(ui, it, a);
           if (kv_len <= 0) continue;
         }
         if (!mbar_wait(bar_s_full(x), s_cnt & 1, abort_flag, a.status, lim)) { ok = false; break; }

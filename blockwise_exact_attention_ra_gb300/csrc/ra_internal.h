@@ -11,6 +11,17 @@
 
 namespace ra {
 
+// Division by a divisor that is fixed for a launch or a work unit, done as a
+// multiply and a shift (the invariant-divisor method of Granlund and
+// Montgomery, "Division by Invariant Integers using Multiplication", 1994):
+// with m = floor(2^40 / d) + 1, floor(n * m / 2^40) = floor(n / d) for all
+// 0 <= n < 2^20 and 1 <= d < 2^20, because the excess n * (m - 2^40 / d) / 2^40
+// stays below 2^-20 < 1 / d.  Tile and iteration indices stay far below 2^20.
+__host__ __device__ inline unsigned long long div_magic(unsigned d) { return (1ull << 40) / d + 1; }
+__host__ __device__ inline int div_by(int n, unsigned long long m) {
+  return (int)(((unsigned long long)(unsigned)n * m) >> 40);
+}
+
 // Rows of a [B, N, H, d] tensor: element (b, n, h, c) sits at
 // b * bstride + (n * H + h) * d + c.
 struct Rows {
@@ -112,6 +123,7 @@ struct TcFwdArgs {
   int causal;
   long long q_off, kv_off;
   int ring_P, ring_S;  // ring mode when ring_P > 0 (Nq == Nkv == P*S, S % 128 == 0)
+  unsigned long long T_m;  // ring mode: div_magic(ring_S / 128)
   int striped;         // ring mode, causal: rows are in striped order (position l*P + host)
   const int* host_len; // ring mode, optional: valid rows per host (device, P entries)
   // outputs
@@ -141,6 +153,7 @@ struct TcBwdArgs {
   int causal;
   int precise;  // two-term fp16 dS in the dK product
   int ring_P, ring_S;
+  unsigned long long T_m;  // div_magic(ring_S / 128)
   int striped;  // causal, rows in striped order (position l*P + host)
   const int* host_len;  // optional: valid rows per host (device, P entries)
   const float* lse;   // [B, Hq, N]: -LSE * log2(e)
