@@ -236,7 +236,6 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kMisc + 4);
   const uint32_t warp = warp_id();
   const uint32_t lane = lane_id();
-  const int group = a.Hq / a.Hkv;
 
   if (threadIdx.x == 0) {
     mbar_init(BAR_KV_FULL, 1);
