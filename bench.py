@@ -31,6 +31,7 @@ if ROOT not in sys.path:
 METRIC = "causal attention TFLOP/s fwd+bwd at 128K bf16 d=128; % of GB300 BF16 peak"
 WORKLOAD = dict(B=1, N=131072, Hq=16, Hkv=16, d=128, P=32, causal=True, cid=3)
 WORKLOAD_NAME = "bf16 causal ring attention fwd+bwd, B1 H16 N131072 d128, P32 virtual hosts of 4096"
+WORKLOAD_OVERRIDDEN = False
 
 
 def algo_flops(B, N, Hq, d, causal=True):
@@ -60,8 +61,11 @@ def load_peaks():
 
 def kernel_traffic(kernel):
     """DRAM bytes per launch from the committed ncu summary, only if it was
-    taken on the current kernel source (sha256 of the .cu file)."""
+    taken on the current kernel source (sha256 of the .cu file) and the
+    workload is the one it was captured on."""
     import hashlib
+    if WORKLOAD_OVERRIDDEN:
+        return None
     src = {"tc_bwd": "ra_bwd_tc.cu", "tc_fwd": "ra_fwd_tc.cu"}[kernel]
     path = os.path.join(ROOT, "blockwise_exact_attention_ra_gb300", "csrc", src)
     sha = hashlib.sha256(open(path, "rb").read()).hexdigest()[:16]
@@ -553,14 +557,21 @@ def main():
     ap.add_argument("--cpu-rows", type=int, default=3072)
     ap.add_argument("--ref-rows", type=int, default=1024)
     ap.add_argument("--N", type=int, default=None, help="override N (profiling on a smaller case)")
-    ap.add_argument("--heads", type=int, default=None, help="override the head count (profiling)")
+    ap.add_argument("--heads", type=int, default=None, help="override the (query) head count")
+    ap.add_argument("--hkv", type=int, default=None, help="override the key/value head count (GQA)")
+    ap.add_argument("--P", type=int, default=None, help="override the number of virtual hosts")
     args = ap.parse_args()
-    if args.N or args.heads:
+    if args.N or args.heads or args.hkv or args.P:
         WORKLOAD["N"] = args.N or WORKLOAD["N"]
         WORKLOAD["Hq"] = WORKLOAD["Hkv"] = args.heads or WORKLOAD["Hq"]
-        global WORKLOAD_NAME
-        WORKLOAD_NAME = (f"bf16 causal ring attention fwd+bwd, B1 H{WORKLOAD['Hq']} N{WORKLOAD['N']} "
-                         f"d128, P32 (profiling case)")
+        WORKLOAD["Hkv"] = args.hkv or WORKLOAD["Hkv"]
+        WORKLOAD["P"] = args.P or WORKLOAD["P"]
+        global WORKLOAD_NAME, WORKLOAD_OVERRIDDEN
+        W = WORKLOAD
+        heads = f"H{W['Hq']}" if W["Hq"] == W["Hkv"] else f"Hq{W['Hq']} Hkv{W['Hkv']}"
+        WORKLOAD_NAME = (f"bf16 causal ring attention fwd+bwd, B1 {heads} N{W['N']} d128, "
+                         f"P{W['P']} virtual hosts of {W['N'] // W['P']} (override of the bench workload)")
+        WORKLOAD_OVERRIDDEN = True
     if args.warmup < 3:
         args.warmup = 3
     ws, rank, local = dist_env()
