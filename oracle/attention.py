@@ -351,12 +351,17 @@ def varlen_rows(N, P, host_len):
 def attention_varlen(q, k, v, do, P, host_len, causal, scale):
     """Exact attention (and, with dO given, its gradients) over the valid rows
     only; padded rows get O = 0, LSE = -inf and zero gradients.  Returns
-    (O, LSE) or (dQ, dK, dV, O, LSE) in the padded layout."""
+    (O, LSE) or (dQ, dK, dV, O, LSE) in the padded layout.  With no valid row
+    at all every row is padding."""
     q, k, v = _f64(q), _f64(k), _f64(v)
     B, N, hq, d = q.shape
     rows = varlen_rows(N, P, host_len)
     O = np.zeros_like(q)
     LSE = np.full((B, hq, N), NEG_INF)
+    if rows.size == 0:
+        if do is None:
+            return O, LSE
+        return np.zeros_like(q), np.zeros_like(k), np.zeros_like(v), O, LSE
     if do is None:
         Ov, Lv = attention_fwd(q[:, rows], k[:, rows], v[:, rows], causal, scale)
         O[:, rows] = Ov

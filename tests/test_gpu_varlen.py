@@ -60,6 +60,13 @@ def test_varlen_tc_head_dim_64_precise(ra):
     _varlen_case(ra, 1, 3 * 256, 2, 1, 64, 3, [200, 256, 5], True, torch.bfloat16, 73, precise=True)
 
 
+@pytest.mark.parametrize("causal", [True, False])
+def test_varlen_all_hosts_empty(ra, causal):
+    # every row is padding: O = 0, LSE = -inf, zero gradients, no tile visited
+    _varlen_case(ra, 1, 4 * 128, 2, 2, 128, 4, [0, 0, 0, 0], causal, torch.bfloat16, 75)
+    _varlen_case(ra, 1, 4 * 64, 2, 2, 64, 4, [0, 0, 0, 0], causal, torch.float32, 76)
+
+
 def test_varlen_fp32(ra):
     _varlen_case(ra, 1, 4 * 64, 2, 2, 64, 4, [64, 10, 0, 33], True, torch.float32, 74)
 

@@ -397,3 +397,15 @@ def test_varlen_empty_host_drops_out(causal):
         np.testing.assert_allclose(g[:, keep], ref, atol=1e-13)
         assert (g[:, S:2 * S] == 0).all()
     assert np.isneginf(L[:, :, S:2 * S]).all()
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_varlen_all_hosts_empty(causal):
+    # no host holds a token: every row is padding, forward and backward
+    P, S = 3, 4
+    q, k, v, do = rand(1, P * S, 2, 3), rand(1, P * S, 2, 3), rand(1, P * S, 2, 3), rand(1, P * S, 2, 3)
+    dq, dk, dv, O, L = oracle.attention_varlen(q, k, v, do, P, [0, 0, 0], causal, 0.9)
+    assert (O == 0).all() and np.isneginf(L).all()
+    assert (dq == 0).all() and (dk == 0).all() and (dv == 0).all()
+    O2, L2 = oracle.attention_varlen(q, k, v, None, P, [0, 0, 0], causal, 0.9)
+    assert (O2 == 0).all() and np.isneginf(L2).all()
