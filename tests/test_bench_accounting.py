@@ -23,3 +23,44 @@ def test_row_flops_sum_to_whole_problem(N, H, d):
     rows_nc = H * sum(bench.row_flops(i, d, False, N) for i in range(N))
     f2, b2 = bench.algo_flops(1, N, H, d, causal=False)
     assert rows_nc == pytest.approx(f2 + b2, rel=1e-12)
+
+
+def _run_bench(args, env_extra=None):
+    import json
+    import os
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    env = dict(os.environ)
+    env.update(env_extra or {})
+    r = subprocess.run([sys.executable, os.path.join(root, "bench.py")] + args, cwd=root, env=env,
+                       capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
+    return [json.loads(ln) for ln in lines]
+
+
+def test_reference_arm_prints_one_contract_line():
+    # the reference arm (the oracle on host cores) on a small override of the workload
+    lines = _run_bench(["--impl", "reference", "--steps", "1", "--warmup", "3", "--ref-rows", "8",
+                        "--N", "2048", "--heads", "2"])
+    assert len(lines) == 1
+    d = lines[0]
+    for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better",
+                "scaling", "vs_baseline", "dtype", "data", "config", "cpu_baseline", "e2e"):
+        assert key in d, key
+    assert d["impl"] == "reference" and d["value"] > 0 and d["warmup"] >= 3
+    assert d["metric"] == bench.METRIC and d["unit"] == "TFLOP/s" and d["higher_is_better"] is True
+    assert "workload" in d["config"] and d["config"]["N"] == 2048
+    cb = d["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == d["value"] and cb["sample"]
+    e = d["e2e"]
+    assert e["value"] == d["value"] and e["unit"] == d["unit"]
+    assert e["h2d_bytes_per_step"] == 0 and e["d2h_bytes_per_step"] == 0
+
+
+def test_reference_arm_other_ranks_exit_quietly():
+    lines = _run_bench(["--impl", "reference", "--steps", "1", "--warmup", "3", "--ref-rows", "8",
+                        "--N", "2048", "--heads", "2"],
+                       {"RANK": "1", "LOCAL_RANK": "1", "WORLD_SIZE": "2", "MASTER_ADDR": "127.0.0.1"})
+    assert lines == []
