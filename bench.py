@@ -140,17 +140,9 @@ class ClockSampler:
         except Exception:
             self.proc = None
 
-    def stop(self):
-        if self.proc is None:
-            return None
-        self.proc.terminate()
-        try:
-            self.proc.wait(timeout=5)
-        except Exception:
-            self.proc.kill()
-        self.file.seek(0)
+    def _parse(self, lines):
         sm, mx, reasons = [], [], set()
-        for line in self.file:
+        for line in lines:
             parts = [p.strip() for p in line.split(",")]
             if len(parts) < 9:
                 continue
@@ -162,10 +154,50 @@ class ClockSampler:
             for name, val in zip(self.NAMES, parts[5:9]):
                 if val.lower() == "active":
                     reasons.add(name)
+        return sm, mx, reasons
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.file.seek(0)
+        sm, mx, reasons = self._parse(self.file)
+        after = False
+        if not sm:
+            # a timed region shorter than nvidia-smi's start-up and first
+            # interval leaves no sample: take one right after it, and say so
+            try:
+                out = subprocess.run(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                                      "-i", str(self.dev)], capture_output=True, text=True, timeout=20).stdout
+            except Exception:
+                out = ""
+            sm, mx, reasons = self._parse(out.splitlines())
+            after = True
         if not sm:
             return None
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
-                "reasons": sorted(reasons)}
+        res = {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
+               "reasons": sorted(reasons)}
+        if after:
+            res["sampled_after_region"] = True
+        return res
+
+
+L2_BYTES = 129 * 2**20  # GB300 last-level cache
+
+
+def l2_note(B, N, Hq, Hkv, d):
+    """How the timed steps stand to L2: each 16-bit input tensor's size."""
+    q_mib = B * N * Hq * d * 2 / 2**20
+    kv_mib = B * N * Hkv * d * 2 / 2**20
+    sizes = (f"Q, K, V, dO {q_mib:.0f} MiB each" if Hq == Hkv else
+             f"Q, dO {q_mib:.0f} MiB, K, V {kv_mib:.0f} MiB each")
+    if min(q_mib, kv_mib) * 2**20 > L2_BYTES:
+        return f"inputs larger than L2 ({sizes}); no flush"
+    return f"inputs not larger than L2 ({sizes}); no flush, so timings include L2 reuse across steps"
 
 
 def max_over_ranks(x, device):
@@ -530,7 +562,7 @@ def run_ours(args, ws, rank, local):
             "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "config": {"workload": WORKLOAD_NAME, "B": B, "N": N, "Hq": Hq, "Hkv": Hkv, "d": d, "P": P,
-                       "causal": True, "l2": "inputs larger than L2 (Q, K, V, dO 512 MiB each); no flush",
+                       "causal": True, "l2": l2_note(B, N, Hq, Hkv, d),
                        "parallelism": "replicas" if ws > 1 else "single GPU"},
             "pct_of_peak": value / ws / peaks["sustained"],
             "fwd_ms": fwd_ms, "bwd_ms": bwd_ms,
