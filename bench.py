@@ -29,7 +29,8 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 METRIC = "causal attention TFLOP/s fwd+bwd at 128K bf16 d=128; % of GB300 BF16 peak"
-WORKLOAD = dict(B=1, N=131072, Hq=16, Hkv=16, d=128, P=32, causal=True, cid=3)
+WORKLOAD = dict(B=1, N=131072, Hq=16, Hkv=16, d=128, P=32, causal=True, cid=3, dtype=torch.bfloat16,
+                q_scale=1.0, v_outlier_frac=0.0, precise=False)
 WORKLOAD_NAME = "bf16 causal ring attention fwd+bwd, B1 H16 N131072 d128, P32 virtual hosts of 4096"
 WORKLOAD_OVERRIDDEN = False
 
@@ -189,10 +190,10 @@ class ClockSampler:
 L2_BYTES = 129 * 2**20  # GB300 last-level cache
 
 
-def l2_note(B, N, Hq, Hkv, d):
-    """How the timed steps stand to L2: each 16-bit input tensor's size."""
-    q_mib = B * N * Hq * d * 2 / 2**20
-    kv_mib = B * N * Hkv * d * 2 / 2**20
+def l2_note(B, N, Hq, Hkv, d, es=2):
+    """How the timed steps stand to L2: each input tensor's size (es bytes per element)."""
+    q_mib = B * N * Hq * d * es / 2**20
+    kv_mib = B * N * Hkv * d * es / 2**20
     sizes = (f"Q, K, V, dO {q_mib:.0f} MiB each" if Hq == Hkv else
              f"Q, dO {q_mib:.0f} MiB, K, V {kv_mib:.0f} MiB each")
     if min(q_mib, kv_mib) * 2**20 > L2_BYTES:
@@ -228,9 +229,12 @@ def cpu_oracle_sample(q, k, v, do, rows, causal, scale):
     (seconds, algorithmic flops of those rows)."""
     import oracle
     heads = sorted({h for _, h, _ in rows})
+    group = q.shape[2] // k.shape[2]   # query heads per key/value head
     hk = {}
     for h in heads:
-        hk[h] = tuple(t[:, :, h:h + 1].float().cpu().numpy().astype(np.float64) for t in (q, k, v, do))
+        g = h // group
+        hk[h] = tuple(t.float().cpu().numpy().astype(np.float64)
+                      for t in (q[:, :, h:h + 1], k[:, :, g:g + 1], v[:, :, g:g + 1], do[:, :, h:h + 1]))
     t0 = time.perf_counter()
     for h in heads:
         qq, kk, vv, dd = hk[h]
@@ -267,13 +271,13 @@ def run_reference(args, ws, rank):
         return
     from blockwise_exact_attention_ra_gb300.inputs import make_tensors
     W = WORKLOAD
-    q, k, v, do = make_tensors(W["B"], W["N"], W["Hq"], W["Hkv"], W["d"], torch.bfloat16, "cpu",
-                               1000 + W["cid"], with_do=True)
+    q, k, v, do = make_tensors(W["B"], W["N"], W["Hq"], W["Hkv"], W["d"], W["dtype"], "cpu",
+                               1000 + W["cid"], W["q_scale"], W["v_outlier_frac"], with_do=True)
     scale = W["d"] ** -0.5
     times, flops = [], []
     for s in range(args.warmup + args.steps):
-        rows = sample_rows(W["N"], W["Hq"], args.ref_rows, 500 + s)
-        dt, fl = cpu_oracle_sample(q, k, v, do, rows, True, scale)
+        rows = sample_rows(W["N"], W["Hq"], min(args.ref_rows, W["N"]), 500 + s)
+        dt, fl = cpu_oracle_sample(q, k, v, do, rows, W["causal"], scale)
         if s >= args.warmup:
             times.append(dt)
             flops.append(fl)
@@ -285,11 +289,12 @@ def run_reference(args, ws, rank):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic",
         "config": {"workload": WORKLOAD_NAME, "B": W["B"], "N": W["N"], "Hq": W["Hq"], "Hkv": W["Hkv"],
-                   "d": W["d"], "P": W["P"], "causal": True, "parallelism": "replicas"},
+                   "d": W["d"], "P": W["P"], "causal": W["causal"], "parallelism": "replicas"},
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
                          "sample": f"{args.ref_rows} seeded query rows of one head per step, fwd+bwd "
                                    f"(incl. their dK/dV contributions), fp64 numpy",
-                         "extrapolated_full_step_s": sum(algo_flops(W["B"], W["N"], W["Hq"], W["d"])) / (value * 1e12),
+                         "extrapolated_full_step_s": sum(algo_flops(W["B"], W["N"], W["Hq"], W["d"], W["causal"]))
+                         / (value * 1e12),
                          "extrapolation": "the workload's algorithmic flops at the sampled rows' rate"},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
@@ -307,30 +312,32 @@ def run_ours(args, ws, rank, local):
         dist.init_process_group("nccl", device_id=dev)
     W = WORKLOAD
     B, N, Hq, Hkv, d, P = W["B"], W["N"], W["Hq"], W["Hkv"], W["d"], W["P"]
+    causal, precise, f32 = W["causal"], W["precise"], W["dtype"] == torch.float32
     scale = d ** -0.5
-    q, k, v, do = make_tensors(B, N, Hq, Hkv, d, torch.bfloat16, dev, 1000 + W["cid"] + 17 * rank)
+    q, k, v, do = make_tensors(B, N, Hq, Hkv, d, W["dtype"], dev, 1000 + W["cid"] + 17 * rank, W["q_scale"],
+                               W["v_outlier_frac"])
     o = torch.empty(B, N, Hq, d, dtype=torch.float32, device=dev)
     lse = torch.empty(B, Hq, N, dtype=torch.float32, device=dev)
     dq = torch.empty(B, N, Hq, d, dtype=torch.float32, device=dev)
     dk = torch.empty(B, N, Hkv, d, dtype=torch.float32, device=dev)
     dv = torch.empty(B, N, Hkv, d, dtype=torch.float32, device=dev)
     sh = ra.shape_of(q, k)
-    wsf = torch.empty(max(16, ra.ra_ring_fwd_workspace_bytes(ra.RA_BF16, sh, P)), dtype=torch.uint8, device=dev)
-    wsb = torch.empty(max(16, ra.ra_ring_bwd_workspace_bytes(ra.RA_BF16, ra.RA_F32, sh, P)),
+    wsf = torch.empty(max(16, ra.ra_ring_fwd_workspace_bytes(ra._dt(q), sh, P)), dtype=torch.uint8, device=dev)
+    wsb = torch.empty(max(16, ra.ra_ring_bwd_workspace_bytes(ra._dt(q), ra.RA_F32, sh, P)),
                       dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
 
     def step(ev=None):
-        ra.ra_ring_fwd(q, k, v, P, True, scale, o, lse, wsf, stream)
+        ra.ra_ring_fwd(q, k, v, P, causal, scale, o, lse, wsf, stream, precise=precise)
         if ev is not None:
             ev.record(stream)
-        ra.ra_ring_bwd(q, k, v, o, do, lse, P, True, scale, dq, dk, dv, wsb, stream)
+        ra.ra_ring_bwd(q, k, v, o, do, lse, P, causal, scale, dq, dk, dv, wsb, stream, precise=precise)
 
     for _ in range(args.warmup):
         step()
     ra.ra_sync_status(stream)
 
-    fwd_fl, bwd_fl = algo_flops(B, N, Hq, d)
+    fwd_fl, bwd_fl = algo_flops(B, N, Hq, d, causal)
     n_ev = args.steps
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(n_ev)]
     mids = [torch.cuda.Event(enable_timing=True) for _ in range(n_ev)]
@@ -359,7 +366,8 @@ def run_ours(args, ws, rank, local):
     total_ms = t_start.elapsed_time(t_end)
     fwd_ms = sum(s.elapsed_time(m) for s, m in zip(starts, mids)) / args.steps
     bwd_ms = sum(m.elapsed_time(e) for m, e in zip(mids, ends)) / args.steps
-    ktime = {kid: ra.ra_kernel_timing_read(kid) for kid in (ra.RA_KERNEL_FWD_TC, ra.RA_KERNEL_BWD_TC)}
+    kfwd, kbwd = (ra.RA_KERNEL_FWD_F32, ra.RA_KERNEL_BWD_F32) if f32 else (ra.RA_KERNEL_FWD_TC, ra.RA_KERNEL_BWD_TC)
+    ktime = {kid: ra.ra_kernel_timing_read(kid) for kid in (kfwd, kbwd)}
     ra.ra_kernel_timing(0)
 
     ms_step = max_over_ranks(total_ms / args.steps, dev)
@@ -367,20 +375,29 @@ def run_ours(args, ws, rank, local):
     peaks = load_peaks()
 
     # dominant kernel: the one with the larger share of device time
-    fwd_k_ms, fwd_n = ktime[ra.RA_KERNEL_FWD_TC]
-    bwd_k_ms, bwd_n = ktime[ra.RA_KERNEL_BWD_TC]
+    fwd_k_ms, fwd_n = ktime[kfwd]
+    bwd_k_ms, bwd_n = ktime[kbwd]
+    kf, kb = ("f32_fwd", "f32_bwd") if f32 else ("tc_fwd", "tc_bwd")
+    if f32:
+        # fp32 CUDA-core kernels: bound by FMA issue; peak = SMs x 128 fp32
+        # lanes x 2 flops x the highest SM clock seen
+        mhz = (clk or {}).get("sm_max_mhz") or 2070.0
+        peak = torch.cuda.get_device_properties(dev).multi_processor_count * 128 * 2 * mhz * 1e6 / 1e12
+        peak_source = f"derived: SMs x 128 fp32 FMA lanes x 2 flops x {mhz:.0f} MHz"
+    else:
+        peak = peaks["sustained"]
+        peak_source = peaks["source"] + ", bf16 sustained (dense fp16 runs at the bf16 rate)"
     kern = {
-        "tc_fwd": {"avg_ms": fwd_k_ms / max(fwd_n, 1), "launches": fwd_n, "flop_per_launch": fwd_fl},
-        "tc_bwd": {"avg_ms": bwd_k_ms / max(bwd_n, 1), "launches": bwd_n, "flop_per_launch": bwd_fl},
+        kf: {"avg_ms": fwd_k_ms / max(fwd_n, 1), "launches": fwd_n, "flop_per_launch": fwd_fl},
+        kb: {"avg_ms": bwd_k_ms / max(bwd_n, 1), "launches": bwd_n, "flop_per_launch": bwd_fl},
     }
     for kk in kern.values():
         kk["tflops"] = kk["flop_per_launch"] / (kk["avg_ms"] * 1e-3) / 1e12
-        kk["frac_of_peak"] = kk["tflops"] / peaks["sustained"]
-    dom = "tc_bwd" if bwd_k_ms >= fwd_k_ms else "tc_fwd"
-    roof = {"bound": "tensor", "kernel": dom, "achieved": kern[dom]["tflops"], "peak": peaks["sustained"],
-            "unit": "TFLOP/s", "frac": kern[dom]["tflops"] / peaks["sustained"],
-            "traffic": kernel_traffic(dom),
-            "peak_source": peaks["source"] + ", bf16 sustained (dense fp16 runs at the bf16 rate)"}
+        kk["frac_of_peak"] = kk["tflops"] / peak
+    dom = kb if bwd_k_ms >= fwd_k_ms else kf
+    roof = {"bound": "alu" if f32 else "tensor", "kernel": dom, "achieved": kern[dom]["tflops"], "peak": peak,
+            "unit": "TFLOP/s", "frac": kern[dom]["tflops"] / peak,
+            "traffic": None if f32 else kernel_traffic(dom), "peak_source": peak_source}
 
     # the striped (load-balanced) causal layout on the same tensors: same
     # algorithmic work, every virtual host with an equal share
@@ -548,23 +565,24 @@ def run_ours(args, ws, rank, local):
 
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
-        rows = sample_rows(N, Hq, args.cpu_rows, 4242)
-        dt, fl = cpu_oracle_sample(q, k, v, do, rows, True, scale)
+        n_rows = min(args.cpu_rows, N)
+        rows = sample_rows(N, Hq, n_rows, 4242)
+        dt, fl = cpu_oracle_sample(q, k, v, do, rows, causal, scale)
         cpu = {"value": fl / dt / 1e12, "unit": "TFLOP/s", "cores": oracle_threads(), "kind": "oracle",
                "extrapolated_full_step_s": (fwd_fl + bwd_fl) / (fl / dt),
                "extrapolation": "the workload's algorithmic flops at the sampled rows' rate",
-               "sample": f"{args.cpu_rows} seeded query rows of one head, fwd+bwd incl. their dK/dV "
+               "sample": f"{n_rows} seeded query rows of one head, fwd+bwd incl. their dK/dV "
                          f"contributions, fp64 numpy; {dt:.1f} s"}
 
     if rank == 0:
         line = {
             "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": ws, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "vs_baseline": None, "dtype": "f32" if f32 else "bf16", "data": "synthetic",
             "config": {"workload": WORKLOAD_NAME, "B": B, "N": N, "Hq": Hq, "Hkv": Hkv, "d": d, "P": P,
-                       "causal": True, "l2": l2_note(B, N, Hq, Hkv, d),
+                       "causal": causal, "l2": l2_note(B, N, Hq, Hkv, d, 4 if f32 else 2),
                        "parallelism": "replicas" if ws > 1 else "single GPU"},
-            "pct_of_peak": value / ws / peaks["sustained"],
+            "pct_of_peak": value / ws / peak,
             "fwd_ms": fwd_ms, "bwd_ms": bwd_ms,
             "fwd_tflops": fwd_fl / (fwd_ms * 1e-3) / 1e12, "bwd_tflops": bwd_fl / (bwd_ms * 1e-3) / 1e12,
             "kernels": kern, "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "striped": striped, "varlen": varlen, "ffn": ffn,
@@ -588,17 +606,32 @@ def main():
     ap.add_argument("--no-ffn", action="store_true", help="skip the blockwise feed-forward measurement")
     ap.add_argument("--cpu-rows", type=int, default=3072)
     ap.add_argument("--ref-rows", type=int, default=1024)
+    ap.add_argument("--config", type=int, choices=[1, 2, 3, 4, 5], default=None,
+                    help="one of the five named workloads (default: 3, the metric's); 4 runs with the "
+                         "two-term fp16 P and dS its outlier inputs need; the striped, variable-length, "
+                         "feed-forward and end-to-end legs belong to workload 3 and are skipped for the others")
     ap.add_argument("--N", type=int, default=None, help="override N (profiling on a smaller case)")
     ap.add_argument("--heads", type=int, default=None, help="override the (query) head count")
     ap.add_argument("--hkv", type=int, default=None, help="override the key/value head count (GQA)")
     ap.add_argument("--P", type=int, default=None, help="override the number of virtual hosts")
     args = ap.parse_args()
+    global WORKLOAD_NAME, WORKLOAD_OVERRIDDEN
+    if args.config is not None:
+        from blockwise_exact_attention_ra_gb300.inputs import CONFIGS
+        c = CONFIGS[args.config]
+        WORKLOAD.update(B=c["B"], N=c["N"], Hq=c["Hq"], Hkv=c["Hkv"], d=c["d"], P=c["P"], causal=c["causal"],
+                        cid=args.config, dtype=c["dtype"], q_scale=c["q_scale"],
+                        v_outlier_frac=c["v_outlier_frac"], precise=args.config == 4)
+        if args.config != 3:
+            WORKLOAD_NAME = (f"workload {args.config}: {c['name']} fwd+bwd, virtual hosts of {c['N'] // c['P']}"
+                             + (", two-term fp16 P and dS" if args.config == 4 else ""))
+            WORKLOAD_OVERRIDDEN = True
+            args.no_striped = args.no_varlen = args.no_ffn = args.no_e2e = True
     if args.N or args.heads or args.hkv or args.P:
         WORKLOAD["N"] = args.N or WORKLOAD["N"]
         WORKLOAD["Hq"] = WORKLOAD["Hkv"] = args.heads or WORKLOAD["Hq"]
         WORKLOAD["Hkv"] = args.hkv or WORKLOAD["Hkv"]
         WORKLOAD["P"] = args.P or WORKLOAD["P"]
-        global WORKLOAD_NAME, WORKLOAD_OVERRIDDEN
         W = WORKLOAD
         heads = f"H{W['Hq']}" if W["Hq"] == W["Hkv"] else f"Hq{W['Hq']} Hkv{W['Hkv']}"
         WORKLOAD_NAME = (f"bf16 causal ring attention fwd+bwd, B1 {heads} N{W['N']} d128, "

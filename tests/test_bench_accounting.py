@@ -64,3 +64,13 @@ def test_reference_arm_other_ranks_exit_quietly():
                         "--N", "2048", "--heads", "2"],
                        {"RANK": "1", "LOCAL_RANK": "1", "WORLD_SIZE": "2", "MASTER_ADDR": "127.0.0.1"})
     assert lines == []
+
+
+def test_reference_arm_named_workload_preset():
+    # workload 1 (fp32, non-causal) through the preset: its sizes and mask reach the line
+    lines = _run_bench(["--impl", "reference", "--config", "1", "--steps", "1", "--warmup", "3",
+                        "--ref-rows", "64"])
+    assert len(lines) == 1
+    c = lines[0]["config"]
+    assert c["N"] == 512 and c["Hq"] == 2 and c["d"] == 64 and c["P"] == 4 and c["causal"] is False
+    assert c["workload"].startswith("workload 1")
