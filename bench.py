@@ -617,8 +617,8 @@ def main():
     args = ap.parse_args()
     global WORKLOAD_NAME, WORKLOAD_OVERRIDDEN
     if args.config is not None:
-        from blockwise_exact_attention_ra_gb300.inputs import CONFIGS
-        c = CONFIGS[args.config]
+        from blockwise_exact_attention_ra_gb300.inputs import WORKLOADS
+        c = WORKLOADS[args.config]
         WORKLOAD.update(B=c["B"], N=c["N"], Hq=c["Hq"], Hkv=c["Hkv"], d=c["d"], P=c["P"], causal=c["causal"],
                         cid=args.config, dtype=c["dtype"], q_scale=c["q_scale"],
                         v_outlier_frac=c["v_outlier_frac"], precise=args.config == 4)

@@ -16,7 +16,7 @@ workload c is 1000 + c.
 """
 import torch
 
-CONFIGS = {
+WORKLOADS = {
     1: dict(name="fp32 non-causal B1 H2 N512 d64 P4", B=1, N=512, Hq=2, Hkv=2, d=64, P=4,
             causal=False, dtype=torch.float32, bwd=True, q_scale=1.0, v_outlier_frac=0.0),
     2: dict(name="bf16 causal B1 H16 N32768 d128 P8", B=1, N=32768, Hq=16, Hkv=16, d=128, P=8,
@@ -66,7 +66,7 @@ def make_tensors(B, N, Hq, Hkv, d, dtype, device, seed, q_scale=1.0, v_outlier_f
 
 
 def make_config(cid, device, with_do=None):
-    c = CONFIGS[cid]
+    c = WORKLOADS[cid]
     if with_do is None:
         with_do = c["bwd"]
     return make_tensors(c["B"], c["N"], c["Hq"], c["Hkv"], c["d"], c["dtype"], device,
@@ -79,7 +79,7 @@ def sample_rows(cid, n_random=512, heads=None, tail=512, seed=None):
     N-1 and the first/last rows of several hosts and 128-row tiles, plus the
     last `tail` rows of one seeded head (which, under a causal mask, are the
     only rows that see the last `tail` keys)."""
-    c = CONFIGS[cid]
+    c = WORKLOADS[cid]
     N, Hq, P = c["N"], c["Hq"], c["P"]
     S = N // P
     g = torch.Generator().manual_seed(7000 + cid if seed is None else seed)

@@ -113,8 +113,8 @@ def _sum_identities(dk, dv, do, group, dtype):
 
 
 def test_fp32_noncausal_N512_full(ra):
-    from blockwise_exact_attention_ra_gb300.inputs import CONFIGS, make_config
-    c = CONFIGS[1]
+    from blockwise_exact_attention_ra_gb300.inputs import WORKLOADS, make_config
+    c = WORKLOADS[1]
     q, k, v, do = make_config(1, "cuda")
     scale = c["d"] ** -0.5
     o, lse = ra.ring_attention_fwd(q, k, v, c["P"], c["causal"], scale)
@@ -127,8 +127,8 @@ def test_fp32_noncausal_N512_full(ra):
 
 
 def test_bf16_causal_N32768_forward_rows(ra):
-    from blockwise_exact_attention_ra_gb300.inputs import CONFIGS, make_config, sample_rows
-    c = CONFIGS[2]
+    from blockwise_exact_attention_ra_gb300.inputs import WORKLOADS, make_config, sample_rows
+    c = WORKLOADS[2]
     q, k, v, _ = make_config(2, "cuda")
     scale = c["d"] ** -0.5
     o, lse = ra.ring_attention_fwd(q, k, v, c["P"], True, scale)
@@ -142,8 +142,8 @@ def test_bf16_causal_N32768_forward_rows(ra):
 
 
 def _fwd_bwd_config(ra, cid, heads, precise, n_random, tail):
-    from blockwise_exact_attention_ra_gb300.inputs import CONFIGS, make_config, sample_rows
-    c = CONFIGS[cid]
+    from blockwise_exact_attention_ra_gb300.inputs import WORKLOADS, make_config, sample_rows
+    c = WORKLOADS[cid]
     group = c["Hq"] // c["Hkv"]
     q, k, v, do = make_config(cid, "cuda")
     scale = c["d"] ** -0.5
