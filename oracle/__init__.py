@@ -10,6 +10,7 @@ from .attention import (  # noqa: F401
     attention_probs,
     attention_bwd,
     attention_rows,
+    attention_bwd_by_row_blocks,
     attention_varlen,
     varlen_rows,
     block_state,

@@ -222,6 +222,83 @@ def attention_rows(q, k, v, rows, causal, scale, do=None, want_kv_grads=False):
     return out
 
 
+def attention_bwd_by_row_blocks(q, k, v, do, causal, scale, keys=None, want_dq=True, row_block=512,
+                                heads=None):
+    """The backward of ``attention_bwd`` for sequences too long for N x N
+    matrices: the query rows are taken ``row_block`` at a time, and every row
+    is still evaluated against all the keys it sees (rows are independent;
+    dK and dV are sums over rows, added one block of rows after another).
+    Under a causal mask the rows of a block see only keys before the block's
+    last row, so the keys after it are not formed at all.
+
+    ``keys``: key rows whose dK, dV are wanted (default all); ``want_dq``:
+    also form dQ (needs dP against every visible key); ``heads``: query heads
+    to include (default all; dK, dV then hold only their contributions).
+    Written with torch fp64 CPU tensors so that the exponentials and products
+    run on every host core.  Returns a dict of float64 numpy arrays: O, LSE,
+    D (as in ``attention_bwd``), dQ (if wanted; zero for heads left out) and
+    dK, dV of shape [B, len(keys), Hkv, d].
+    """
+    import torch
+    t = [torch.as_tensor(np.asarray(x, dtype=np.float64)) for x in (q, k, v, do)]
+    q, k, v, do = t
+    B, n, hq, d = q.shape
+    nk, hkv = k.shape[1], k.shape[2]
+    keys = torch.arange(nk) if keys is None else torch.as_tensor(np.asarray(keys, dtype=np.int64))
+    all_keys = keys.numel() == nk and bool((keys == torch.arange(nk)).all())
+    heads = range(hq) if heads is None else heads
+    O = torch.zeros(B, n, hq, d, dtype=torch.float64)
+    LSE = torch.full((B, hq, n), NEG_INF, dtype=torch.float64)
+    D = torch.zeros(B, hq, n, dtype=torch.float64)
+    dQ = torch.zeros(B, n, hq, d, dtype=torch.float64) if want_dq else None
+    dK = torch.zeros(B, keys.numel(), hkv, d, dtype=torch.float64)
+    dV = torch.zeros(B, keys.numel(), hkv, d, dtype=torch.float64)
+    for b in range(B):
+        for h in heads:
+            g = _kv_head(h, hq, hkv)
+            kk, vv = k[b, :, g], v[b, :, g]
+            for r0 in range(0, n, row_block):
+                r1 = min(n, r0 + row_block)
+                kend = min(r1, nk) if causal else nk  # keys any row of the block can see
+                sel_pos = torch.nonzero(keys < kend).flatten()
+                if not want_dq and sel_pos.numel() == 0:
+                    continue
+                qc, dc = q[b, r0:r1, h], do[b, r0:r1, h]
+                s = scale * (qc @ kk[:kend].T)
+                if causal:
+                    vis = torch.arange(kend)[None, :] <= torch.arange(r0, r1)[:, None]
+                    s = torch.where(vis, s, torch.tensor(NEG_INF, dtype=torch.float64))
+                m = s.max(dim=1).values
+                ok = torch.isfinite(m)
+                lse = torch.full_like(m, NEG_INF)
+                lse[ok] = m[ok] + torch.log(torch.exp(s[ok] - m[ok, None]).sum(dim=1))
+                P = torch.zeros_like(s)
+                P[ok] = torch.exp(s[ok] - lse[ok, None])
+                del s
+                o = P @ vv[:kend]
+                Dr = (dc * o).sum(dim=1)
+                O[b, r0:r1, h], LSE[b, h, r0:r1], D[b, h, r0:r1] = o, lse, Dr
+                if want_dq or all_keys:
+                    dS = P * (dc @ vv[:kend].T - Dr[:, None])
+                    if want_dq:
+                        dQ[b, r0:r1, h] = scale * (dS @ kk[:kend])
+                    if all_keys:
+                        dK[b, :kend, g] += scale * (dS.T @ qc)
+                        dV[b, :kend, g] += P.T @ dc
+                        continue
+                    del dS
+                if sel_pos.numel():
+                    sk = keys[sel_pos]
+                    Ps = P[:, sk]
+                    dSs = Ps * (dc @ vv[sk].T - Dr[:, None])
+                    dK[b, sel_pos, g] += scale * (dSs.T @ qc)
+                    dV[b, sel_pos, g] += Ps.T @ dc
+    out = {"O": O.numpy(), "LSE": LSE.numpy(), "D": D.numpy(), "dK": dK.numpy(), "dV": dV.numpy()}
+    if want_dq:
+        out["dQ"] = dQ.numpy()
+    return out
+
+
 # ---------------------------------------------------------------------------
 # Blockwise mode: the ring schedule and the rescaled (max, exp_sum,
 # weighted_output) merge.  Used to pin the merge algebra against the plain

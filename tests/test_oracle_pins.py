@@ -409,3 +409,51 @@ def test_varlen_all_hosts_empty(causal):
     assert (dq == 0).all() and (dk == 0).all() and (dv == 0).all()
     O2, L2 = oracle.attention_varlen(q, k, v, None, P, [0, 0, 0], causal, 0.9)
     assert (O2 == 0).all() and np.isneginf(L2).all()
+
+
+# --- the row-block mode of the backward against the full matrices ---------------
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("row_block", [1, 7, 64])
+def test_row_block_backward_matches_full(causal, row_block):
+    B, N, hq, hkv, d = 2, 37, 4, 2, 5
+    q, k, v, do = rand(B, N, hq, d), rand(B, N, hkv, d), rand(B, N, hkv, d), rand(B, N, hq, d)
+    dq, dk, dv, O, LSE, D = oracle.attention_bwd(q, k, v, do, causal, 0.45)
+    r = oracle.attention_bwd_by_row_blocks(q, k, v, do, causal, 0.45, row_block=row_block)
+    for name, got, want in (("O", r["O"], O), ("LSE", r["LSE"], LSE), ("D", r["D"], D), ("dQ", r["dQ"], dq),
+                            ("dK", r["dK"], dk), ("dV", r["dV"], dv)):
+        np.testing.assert_allclose(got, want, atol=1e-12, err_msg=name)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_row_block_backward_selected_keys_and_heads(causal):
+    B, N, hq, hkv, d = 1, 50, 4, 2, 6
+    q, k, v, do = rand(B, N, hq, d), rand(B, N, hkv, d), rand(B, N, hkv, d), rand(B, N, hq, d)
+    keys = np.array([0, 3, 17, 31, 32, 49])
+    dq, dk, dv, *_ = oracle.attention_bwd(q, k, v, do, causal, 0.6)
+    r = oracle.attention_bwd_by_row_blocks(q, k, v, do, causal, 0.6, keys=keys, want_dq=False, row_block=16)
+    np.testing.assert_allclose(r["dK"], dk[:, keys], atol=1e-12)
+    np.testing.assert_allclose(r["dV"], dv[:, keys], atol=1e-12)
+    assert "dQ" not in r
+    # the heads of key/value head 1 only: its dK, dV are complete, head 0's are zero
+    r1 = oracle.attention_bwd_by_row_blocks(q, k, v, do, causal, 0.6, keys=keys, heads=[2, 3], row_block=9)
+    np.testing.assert_allclose(r1["dK"][:, :, 1], dk[:, keys, 1], atol=1e-12)
+    np.testing.assert_allclose(r1["dV"][:, :, 1], dv[:, keys, 1], atol=1e-12)
+    assert not r1["dK"][:, :, 0].any() and not r1["dV"][:, :, 0].any()
+
+
+def test_row_block_backward_key_gradient_by_finite_differences():
+    # dK and dV of one selected key against central differences of L = sum(O * dO)
+    B, N, hq, hkv, d = 1, 9, 2, 1, 3
+    q, k, v, do = rand(B, N, hq, d), rand(B, N, hkv, d), rand(B, N, hkv, d), rand(B, N, hq, d)
+    j, eps = 4, 1e-6
+    r = oracle.attention_bwd_by_row_blocks(q, k, v, do, True, 0.7, keys=[j], want_dq=False, row_block=2)
+    for name, x, g in (("k", k, r["dK"]), ("v", v, r["dV"])):
+        for c in range(d):
+            xp, xm = x.copy(), x.copy()
+            xp[0, j, 0, c] += eps
+            xm[0, j, 0, c] -= eps
+            kp, vp = (xp, v) if name == "k" else (k, xp)
+            km, vm = (xm, v) if name == "k" else (k, xm)
+            num = (_loss(q, kp, vp, do, True, 0.7) - _loss(q, km, vm, do, True, 0.7)) / (2 * eps)
+            assert abs(g[0, 0, 0, c] - num) < 1e-7 * max(1.0, abs(num)), (name, c)
