@@ -6,7 +6,10 @@ oracle, so they are checked (a) on seeded query rows computed one by one by
 the oracle (O, LSE, dQ), (b) on the last 512 keys of a seeded head, whose
 dK and dV depend under a causal mask only on the last 512 query rows (of
 every query head of the group) and are therefore exact from those rows, and
-(c) on identities that hold at any size: sum_j dK_j = 0 (the rows of dS sum
+(c) at the bench workload, on three whole key tiles inside the sequence
+(host 0's first tile and the two tiles beside the boundary between hosts
+15 and 16), whose dK and dV the oracle forms from every query row that sees
+them, and (d) on identities that hold at any size: sum_j dK_j = 0 (the rows of dS sum
 to zero) and sum_j dV_j = sum_i dO_i (the rows of P sum to one), per
 key/value head and column, in fp64 on the GPU's outputs.
 """
@@ -141,7 +144,7 @@ def test_bf16_causal_N32768_forward_rows(ra):
     _free()
 
 
-def _fwd_bwd_config(ra, cid, heads, precise, n_random, tail):
+def _fwd_bwd_config(ra, cid, heads, precise, n_random, tail, interior=None):
     from blockwise_exact_attention_ra_gb300.inputs import WORKLOADS, make_config, sample_rows
     c = WORKLOADS[cid]
     group = c["Hq"] // c["Hkv"]
@@ -164,12 +167,25 @@ def _fwd_bwd_config(ra, cid, heads, precise, n_random, tail):
     check(f"{c['name']} tail dQ", _gpu_rows(dq, order_t), rt["dQ"], c["dtype"])
     check(f"{c['name']} tail dK", f64(dk[0, N - tail:, g]), kvg[g][0][N - tail:], c["dtype"])
     check(f"{c['name']} tail dV", f64(dv[0, N - tail:, g]), kvg[g][1][N - tail:], c["dtype"])
+    if interior:
+        # whole key tiles inside the sequence: every query row that sees them
+        # (all rows at or after the tile) evaluated by the oracle, one block of
+        # rows at a time; these are the key tiles with the most visitors
+        keys = np.concatenate([np.arange(t0, t0 + 128) for t0 in interior])
+        hs = list(range(g * group, (g + 1) * group))
+        r = oracle.attention_bwd_by_row_blocks(f64(q[:, :, hs]), _head64(k, g), _head64(v, g), f64(do[:, :, hs]),
+                                               True, scale, keys=keys, want_dq=False)
+        check(f"{c['name']} interior dK", f64(dk[0, keys, g]), r["dK"][0, :, 0], c["dtype"])
+        check(f"{c['name']} interior dV", f64(dv[0, keys, g]), r["dV"][0, :, 0], c["dtype"])
     del q, k, v, do, o, lse, dq, dk, dv
     _free()
 
 
 def test_bf16_causal_N131072_fwd_bwd(ra):
-    _fwd_bwd_config(ra, 3, heads=[1, 6, 11, 15], precise=False, n_random=512, tail=512)
+    # interior key tiles: host 0's first tile (seen by all 131072 query rows) and
+    # the last tile of host 15 with the first of host 16 (the ring's midpoint)
+    _fwd_bwd_config(ra, 3, heads=[1, 6, 11, 15], precise=False, n_random=512, tail=512,
+                    interior=[0, 16 * 4096 - 128, 16 * 4096])
 
 
 def test_bf16_gqa_stress_N262144_fwd_bwd(ra):

@@ -259,3 +259,26 @@ def test_fp16_range_overflow_is_reported(ra):
         ra.ra_sync_status()
     assert e.value.code == 4
     ra.ra_sync_status()
+
+
+def test_tc_ring_values_below_fp16_normal_range(ra):
+    # V and dO scaled by 1e-5 sit below fp16's smallest normal (2^-14 ~ 6.1e-5):
+    # their fp16 operand copies are subnormal and round to a multiple of 2^-24
+    # without a status error; every output stays within the absolute bf16
+    # tolerances.  O and dV also keep a small error relative to their own size;
+    # dQ and dK do not (dS ~ 1e-10 here is below fp16's subnormals and rounds
+    # to zero), which the absolute bound allows
+    q, k, v, do = _inputs(1, 1024, 2, 2, 128, torch.bfloat16, 44)
+    v = (v.float() * 1e-5).to(torch.bfloat16)
+    do = (do.float() * 1e-5).to(torch.bfloat16)
+    scale = 128 ** -0.5
+    o, lse = ra.ring_attention_fwd(q, k, v, 4, True, scale)
+    dq, dk, dv = ra.ring_attention_bwd(q, k, v, o, lse, do, 4, True, scale)
+    ra.ra_sync_status()
+    rq, rk, rv, rO, rL, _ = oracle.attention_bwd(f64(q), f64(k), f64(v), f64(do), True, scale)
+    for name, got, want in (("O", o, rO), ("dQ", dq, rq), ("dK", dk, rk), ("dV", dv, rv)):
+        check(f"tiny {name}", f64(got), want, torch.bfloat16)
+        if name in ("O", "dV"):
+            rel = np.abs(f64(got) - want).max() / np.abs(want).max()
+            assert rel < 2e-2, f"tiny {name}: error {rel:.3e} of the largest entry"
+    check("tiny LSE", f64(lse), rL, torch.bfloat16, kind="lse")
