@@ -265,6 +265,16 @@ def sample_rows(N, Hq, count, seed):
     return [(0, h, int(i)) for i in idx]
 
 
+def bench_config(ws):
+    """The `config` object of the JSON line, the same for both arms."""
+    W = WORKLOAD
+    f32 = W["dtype"] == torch.float32
+    return {"workload": WORKLOAD_NAME, "B": W["B"], "N": W["N"], "Hq": W["Hq"], "Hkv": W["Hkv"], "d": W["d"],
+            "P": W["P"], "causal": W["causal"],
+            "l2": l2_note(W["B"], W["N"], W["Hq"], W["Hkv"], W["d"], 4 if f32 else 2),
+            "parallelism": "replicas" if ws > 1 else "single GPU"}
+
+
 def run_reference(args, ws, rank):
     """Reference arm: the fp64 oracle on the host cores, bounded row samples."""
     if rank != 0:
@@ -288,8 +298,7 @@ def run_reference(args, ws, rank):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * sum(times) / len(times),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic",
-        "config": {"workload": WORKLOAD_NAME, "B": W["B"], "N": W["N"], "Hq": W["Hq"], "Hkv": W["Hkv"],
-                   "d": W["d"], "P": W["P"], "causal": W["causal"], "parallelism": "replicas"},
+        "config": bench_config(ws),
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
                          "sample": f"{args.ref_rows} seeded query rows of one head per step, fwd+bwd "
                                    f"(incl. their dK/dV contributions), fp64 numpy",
@@ -555,12 +564,35 @@ def run_ours(args, ws, rank, local):
         torch.cuda.synchronize(dev)
         ra.ra_sync_status(main)
         e_ms = max_over_ranks(a.elapsed_time(b) / args.steps, dev)
+        h2d_bytes = sum(t.numel() * t.element_size() for t in host_in)
+        d2h_bytes = sum(t.numel() * t.element_size() for t in host_out[0])
+        # what sets the pace: the same steps again with the library's event
+        # timing on, which brackets every copy group and every kernel on its own
+        # stream (a separate pass, so the timed steps above carry no events)
+        ra.ra_kernel_timing(1)
+        e2e_steps(args.steps)
+        for st_ in sts:
+            main.wait_stream(st_)
+        torch.cuda.synchronize(dev)
+        part = {name: ra.ra_kernel_timing_read(kid)[0] / args.steps for name, kid in
+                (("h2d", ra.RA_COPY_H2D), ("d2h", ra.RA_COPY_D2H), ("fwd", ra.RA_KERNEL_FWD_TC),
+                 ("bwd", ra.RA_KERNEL_BWD_TC))}
+        ra.ra_kernel_timing(0)
+        kern_ms, copy_ms = part["fwd"] + part["bwd"], part["h2d"] + part["d2h"]
         e2e = {"value": job_value(ws, fwd_fl + bwd_fl, e_ms), "unit": "TFLOP/s",
                "ms_per_step": e_ms,
-               "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in host_in),
-               "d2h_bytes_per_step": sum(t.numel() * t.element_size() for t in host_out[0]),
+               "h2d_bytes_per_step": h2d_bytes,
+               "d2h_bytes_per_step": d2h_bytes,
                "api": "ra_ring_step_host (host buffers, pinned), two streams alternating",
-               "host_memory": arena.kind}
+               "host_memory": arena.kind,
+               "breakdown": {
+                   "h2d_ms_per_step": part["h2d"], "d2h_ms_per_step": part["d2h"],
+                   "h2d_gbs": h2d_bytes / (part["h2d"] * 1e-3) / 1e9 if part["h2d"] > 0 else None,
+                   "d2h_gbs": d2h_bytes / (part["d2h"] * 1e-3) / 1e9 if part["d2h"] > 0 else None,
+                   "kernel_ms_per_step": kern_ms, "copy_ms_per_step": copy_ms,
+                   "bound_by": "copies" if copy_ms > kern_ms else "kernels",
+                   "how": "CUDA events around each copy group and each attention kernel on its own stream, "
+                          "a second pass of the same steps"}}
         del wsh
 
     cpu = None
@@ -579,9 +611,7 @@ def run_ours(args, ws, rank, local):
             "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": ws, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f32" if f32 else "bf16", "data": "synthetic",
-            "config": {"workload": WORKLOAD_NAME, "B": B, "N": N, "Hq": Hq, "Hkv": Hkv, "d": d, "P": P,
-                       "causal": causal, "l2": l2_note(B, N, Hq, Hkv, d, 4 if f32 else 2),
-                       "parallelism": "replicas" if ws > 1 else "single GPU"},
+            "config": bench_config(ws),
             "pct_of_peak": value / ws / peak,
             "fwd_ms": fwd_ms, "bwd_ms": bwd_ms,
             "fwd_tflops": fwd_fl / (fwd_ms * 1e-3) / 1e12, "bwd_tflops": bwd_fl / (bwd_ms * 1e-3) / 1e12,

@@ -2,8 +2,11 @@
 
 Argument marshalling only: every step of the computation runs in the CUDA
 kernels behind the C ABI declared in include/ra.h.  PyTorch supplies device
-memory and streams.  Importing this package without the compiled library
-raises ImportError; there is no other implementation to fall back to.
+memory and streams.  The compiled library is loaded on first use (the first
+call, or the first access to ``lib``), so that importing the package for its
+seeded input generators maps no product code; if the library is missing that
+first use raises ImportError.  There is no other implementation to fall back
+to.
 
 Functions with the C names (``ra_block_fwd``, ``ra_merge``, ``ra_ring_fwd``,
 ``ra_ring_bwd``, ...) take torch tensors in the [B, N, H, d] layout and raise
@@ -12,6 +15,7 @@ additionally allocate outputs and workspace with torch.
 """
 import ctypes
 import os
+import threading
 
 import torch
 
@@ -21,7 +25,7 @@ __all__ = [
     "ra_ring_fwd", "ra_ring_fwd_workspace_bytes", "ra_ring_bwd", "ra_ring_bwd_workspace_bytes",
     "ra_ring_fwd_noalloc", "ra_ring_fwd_varlen", "ra_ring_bwd_varlen", "ra_ring_step_host",
     "ra_ring_step_host_workspace_bytes", "ra_ffn_workspace_bytes", "ra_ffn_fwd", "ra_ffn_bwd",
-    "ra_sync_status", "ra_last_error", "ra_launch_count", "ra_selftest_timeout",
+    "ra_sync_status", "ra_last_error", "ra_launch_count", "ra_selftest_timeout", "ra_debug_visit_log",
     "ra_kernel_timing", "ra_kernel_timing_read",
     "ring_attention_fwd", "ring_attention_bwd", "RA_F32", "RA_BF16", "RA_F16",
     "RA_CAUSAL", "RA_PRECISE", "RA_STRIPED",
@@ -80,6 +84,7 @@ def _load():
         "ra_sync_status": (i, [vp]),
         "ra_last_error": (ctypes.c_char_p, []),
         "ra_launch_count": (ctypes.c_ulonglong, []),
+        "ra_debug_visit_log": (i, [vp, sz, vp]),
         "ra_selftest_timeout": (i, [ctypes.c_uint, vp]),
         "ra_kernel_timing": (i, [i]),
         "ra_kernel_timing_read": (i, [i, ctypes.POINTER(ctypes.c_double),
@@ -92,15 +97,32 @@ def _load():
     return L
 
 
-lib = _load()
+_LIB = None
+_LIB_LOCK = threading.Lock()
+
+
+def _lib():
+    """The loaded library (loaded on the first call)."""
+    global _LIB
+    if _LIB is None:
+        with _LIB_LOCK:
+            if _LIB is None:
+                _LIB = _load()
+    return _LIB
+
+
+def __getattr__(name):
+    if name == "lib":
+        return _lib()
+    raise AttributeError(f"module {__name__!r} has no attribute {name!r}")
 
 
 def ra_last_error():
-    return lib.ra_last_error().decode()
+    return _lib().ra_last_error().decode()
 
 
 def ra_launch_count():
-    return int(lib.ra_launch_count())
+    return int(_lib().ra_launch_count())
 
 
 def _check(code):
@@ -149,34 +171,47 @@ def shape_of(q, k):
 
 
 RA_KERNEL_FWD_TC, RA_KERNEL_BWD_TC, RA_KERNEL_FWD_F32, RA_KERNEL_BWD_F32, RA_KERNEL_GEMM_TC = 0, 1, 2, 3, 4
+RA_COPY_H2D, RA_COPY_D2H = 5, 6
 
 
 def ra_kernel_timing(enable):
-    _check(lib.ra_kernel_timing(int(bool(enable))))
+    _check(_lib().ra_kernel_timing(int(bool(enable))))
 
 
 def ra_kernel_timing_read(kernel):
     """(total device ms, launches) of one kernel since timing was enabled."""
     ms = ctypes.c_double()
     n = ctypes.c_ulonglong()
-    _check(lib.ra_kernel_timing_read(int(kernel), ctypes.byref(ms), ctypes.byref(n)))
+    _check(_lib().ra_kernel_timing_read(int(kernel), ctypes.byref(ms), ctypes.byref(n)))
     return ms.value, int(n.value)
 
 
+def ra_debug_visit_log(entries, count):
+    """Start recording the ring schedule into `entries` (int32 device tensor
+    [capacity, 4]) and `count` (one zeroed int32 device element); pass None
+    for both to stop.  See include/ra.h."""
+    if entries is None:
+        _check(_lib().ra_debug_visit_log(None, 0, None))
+        return
+    if entries.dim() != 2 or entries.shape[1] != 4 or entries.element_size() != 4 or not entries.is_contiguous():
+        raise RAError(1, "visit log entries must be a contiguous [capacity, 4] tensor of 32-bit integers")
+    _check(_lib().ra_debug_visit_log(_ptr(entries), entries.shape[0], _ptr(count)))
+
+
 def ra_sync_status(stream=None):
-    _check(lib.ra_sync_status(_stream(stream)))
+    _check(_lib().ra_sync_status(_stream(stream)))
 
 
 def ra_selftest_timeout(timeout_us, stream=None):
-    _check(lib.ra_selftest_timeout(int(timeout_us), _stream(stream)))
+    _check(_lib().ra_selftest_timeout(int(timeout_us), _stream(stream)))
 
 
 def ra_acc_init(o_acc, m_acc, l_acc, shape, stream=None):
-    _check(lib.ra_acc_init(_ptr(o_acc), _ptr(m_acc), _ptr(l_acc), shape, _stream(stream)))
+    _check(_lib().ra_acc_init(_ptr(o_acc), _ptr(m_acc), _ptr(l_acc), shape, _stream(stream)))
 
 
 def ra_block_fwd_workspace_bytes(dtype, shape):
-    return int(lib.ra_block_fwd_workspace_bytes(dtype, shape))
+    return int(_lib().ra_block_fwd_workspace_bytes(dtype, shape))
 
 
 def ra_block_fwd(q, k_blk, v_blk, o_acc, m_acc, l_acc, q_off, kv_off, causal, scale,
@@ -185,30 +220,30 @@ def ra_block_fwd(q, k_blk, v_blk, o_acc, m_acc, l_acc, q_off, kv_off, causal, sc
     shape = shape or shape_of(q, k_blk)
     dt = _dt(q)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
-    _check(lib.ra_block_fwd(_ptr(q), _ptr(k_blk), _ptr(v_blk), dt, _ptr(o_acc), _ptr(m_acc),
+    _check(_lib().ra_block_fwd(_ptr(q), _ptr(k_blk), _ptr(v_blk), dt, _ptr(o_acc), _ptr(m_acc),
                             _ptr(l_acc), shape, int(q_off), int(kv_off), _flags(causal, precise),
                             float(scale), _ptr(workspace), ws_bytes, _stream(stream)))
 
 
 def ra_merge(o_a, m_a, l_a, o_b, m_b, l_b, shape, stream=None):
-    _check(lib.ra_merge(_ptr(o_a), _ptr(m_a), _ptr(l_a), _ptr(o_b), _ptr(m_b), _ptr(l_b),
+    _check(_lib().ra_merge(_ptr(o_a), _ptr(m_a), _ptr(l_a), _ptr(o_b), _ptr(m_b), _ptr(l_b),
                         shape, _stream(stream)))
 
 
 def ra_finalize(o_acc, m_acc, l_acc, o_out, lse, shape, stream=None):
-    _check(lib.ra_finalize(_ptr(o_acc), _ptr(m_acc), _ptr(l_acc), _ptr(o_out), _dt(o_out),
+    _check(_lib().ra_finalize(_ptr(o_acc), _ptr(m_acc), _ptr(l_acc), _ptr(o_out), _dt(o_out),
                            _ptr(lse), shape, _stream(stream)))
 
 
 def ra_ring_fwd_workspace_bytes(dtype, shape, P):
-    return int(lib.ra_ring_fwd_workspace_bytes(dtype, shape, P))
+    return int(_lib().ra_ring_fwd_workspace_bytes(dtype, shape, P))
 
 
 def ra_ring_fwd(q, k, v, P, causal, scale, o, lse, workspace=None, stream=None, precise=False,
                 striped=False):
     shape = shape_of(q, k)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
-    _check(lib.ra_ring_fwd(_ptr(q), _ptr(k), _ptr(v), _dt(q), shape, int(P), _flags(causal, precise, striped),
+    _check(_lib().ra_ring_fwd(_ptr(q), _ptr(k), _ptr(v), _dt(q), shape, int(P), _flags(causal, precise, striped),
                            float(scale), _ptr(o), _dt(o), _ptr(lse), _ptr(workspace), ws_bytes,
                            _stream(stream)))
 
@@ -219,7 +254,7 @@ def ra_ring_fwd_noalloc(q, k, v, P, causal, scale, o, lse, stream=None, precise=
     (shapes needing more are rejected).  Calls that overlap on the GPU race on
     that buffer."""
     shape = shape_of(q, k)
-    _check(lib.ra_ring_fwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _dt(q), shape, int(P),
+    _check(_lib().ra_ring_fwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _dt(q), shape, int(P),
                                    _flags(causal, precise, striped), float(scale), _ptr(o), _dt(o),
                                    _ptr(lse), _stream(stream)))
 
@@ -230,7 +265,7 @@ def ra_ring_fwd_varlen(q, k, v, P, host_len, causal, scale, o, lse, workspace=No
     int32 device tensor of P entries) and the rest is padding."""
     shape = shape_of(q, k)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
-    _check(lib.ra_ring_fwd_varlen(_ptr(q), _ptr(k), _ptr(v), _dt(q), shape, int(P), _ptr(host_len),
+    _check(_lib().ra_ring_fwd_varlen(_ptr(q), _ptr(k), _ptr(v), _dt(q), shape, int(P), _ptr(host_len),
                                   _flags(causal, precise), float(scale), _ptr(o), _dt(o), _ptr(lse),
                                   _ptr(workspace), ws_bytes, _stream(stream)))
 
@@ -239,14 +274,14 @@ def ra_ring_bwd_varlen(q, k, v, o, dO, lse, P, host_len, causal, scale, dq, dk, 
                        stream=None, precise=False):
     shape = shape_of(q, k)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
-    _check(lib.ra_ring_bwd_varlen(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _dt(o), _ptr(dO), _ptr(lse),
+    _check(_lib().ra_ring_bwd_varlen(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _dt(o), _ptr(dO), _ptr(lse),
                                   _dt(q), shape, int(P), _ptr(host_len), _flags(causal, precise),
                                   float(scale), _ptr(dq), _ptr(dk), _ptr(dv), _dt(dq), _ptr(workspace),
                                   ws_bytes, _stream(stream)))
 
 
 def ra_ring_step_host_workspace_bytes(dtype, o_dtype, grad_dtype, shape, P):
-    return int(lib.ra_ring_step_host_workspace_bytes(dtype, o_dtype, grad_dtype, shape, int(P)))
+    return int(_lib().ra_ring_step_host_workspace_bytes(dtype, o_dtype, grad_dtype, shape, int(P)))
 
 
 def ra_ring_step_host(q, k, v, dO, P, causal, scale, o, lse, dq, dk, dv, workspace, stream=None,
@@ -267,14 +302,14 @@ def ra_ring_step_host(q, k, v, dO, P, causal, scale, o, lse, dq, dk, dv, workspa
         raise RAError(1, "ra_ring_step_host: lse must be packed [B, Hq, N]")
     shape = shape_of(q, k)
     ws_bytes = workspace.numel() * workspace.element_size()
-    _check(lib.ra_ring_step_host(_ptr(q), _ptr(k), _ptr(v), _ptr(dO), _dt(q), shape, int(P),
+    _check(_lib().ra_ring_step_host(_ptr(q), _ptr(k), _ptr(v), _ptr(dO), _dt(q), shape, int(P),
                                  _flags(causal, precise, striped), float(scale), _ptr(o), _dt(o),
                                  _ptr(lse), _ptr(dq), _ptr(dk), _ptr(dv), _dt(dq), _ptr(workspace),
                                  ws_bytes, _stream(stream)))
 
 
 def ra_ffn_workspace_bytes(dtype, T, d_model, d_hidden, block, backward):
-    return int(lib.ra_ffn_workspace_bytes(dtype, int(T), int(d_model), int(d_hidden), int(block),
+    return int(_lib().ra_ffn_workspace_bytes(dtype, int(T), int(d_model), int(d_hidden), int(block),
                                           1 if backward else 0))
 
 
@@ -294,14 +329,14 @@ def _ffn_check(x, w1, w2):
 def ra_ffn_fwd(x, w1, w2, block, y, workspace, stream=None):
     """y = GELU(x w1^T) w2^T one block of `block` tokens at a time."""
     T, dm, dh = _ffn_check(x, w1, w2)
-    _check(lib.ra_ffn_fwd(_ptr(x), _ptr(w1), _ptr(w2), _dt(x), T, dm, dh, int(block), _ptr(y), _dt(y),
+    _check(_lib().ra_ffn_fwd(_ptr(x), _ptr(w1), _ptr(w2), _dt(x), T, dm, dh, int(block), _ptr(y), _dt(y),
                           _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream)))
 
 
 def ra_ffn_bwd(x, w1, w2, dy, block, dx, dw1, dw2, workspace, stream=None):
     """Gradients of sum(y * dy): dx, and fp32 dw1, dw2 (overwritten)."""
     T, dm, dh = _ffn_check(x, w1, w2)
-    _check(lib.ra_ffn_bwd(_ptr(x), _ptr(w1), _ptr(w2), _ptr(dy), _dt(x), T, dm, dh, int(block), _ptr(dx),
+    _check(_lib().ra_ffn_bwd(_ptr(x), _ptr(w1), _ptr(w2), _ptr(dy), _dt(x), T, dm, dh, int(block), _ptr(dx),
                           _dt(dx), _ptr(dw1), _ptr(dw2), _ptr(workspace),
                           workspace.numel() * workspace.element_size(), _stream(stream)))
 
@@ -328,14 +363,14 @@ def ffn_bwd(x, w1, w2, dy, block=None, dx_dtype=torch.float32, stream=None):
 
 
 def ra_ring_bwd_workspace_bytes(dtype, grad_dtype, shape, P):
-    return int(lib.ra_ring_bwd_workspace_bytes(dtype, grad_dtype, shape, P))
+    return int(_lib().ra_ring_bwd_workspace_bytes(dtype, grad_dtype, shape, P))
 
 
 def ra_ring_bwd(q, k, v, o, dO, lse, P, causal, scale, dq, dk, dv, workspace, stream=None,
                 precise=False, striped=False):
     shape = shape_of(q, k)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
-    _check(lib.ra_ring_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _dt(o), _ptr(dO), _ptr(lse),
+    _check(_lib().ra_ring_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _dt(o), _ptr(dO), _ptr(lse),
                            _dt(q), shape, int(P), _flags(causal, precise, striped), float(scale), _ptr(dq),
                            _ptr(dk), _ptr(dv), _dt(dq), _ptr(workspace), ws_bytes,
                            _stream(stream)))

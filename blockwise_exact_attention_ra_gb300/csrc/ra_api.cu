@@ -291,6 +291,16 @@ int set_error(int code, const char* msg) {
   return code;
 }
 
+namespace {
+// The debug visit log set by ra_debug_visit_log (process-wide; off by default).
+std::mutex g_log_mu;
+VisitLog g_log{nullptr, nullptr, 0};
+VisitLog visit_log() {
+  std::lock_guard<std::mutex> lk(g_log_mu);
+  return g_log;
+}
+}  // namespace
+
 }  // namespace ra
 
 using namespace ra;
@@ -301,6 +311,19 @@ extern "C" {
 const char* ra_last_error(void) { return t_err.c_str(); }
 
 unsigned long long ra_launch_count(void) { return g_launches.load(); }
+
+int ra_debug_visit_log(unsigned int* entries, size_t capacity, unsigned int* count) {
+  if (entries && (!count || capacity == 0))
+    return fail(RA_ERR_INVALID_ARG, "a visit log needs a count word and a capacity > 0");
+  if (entries && ((reinterpret_cast<uintptr_t>(entries) & 15u) || (reinterpret_cast<uintptr_t>(count) & 3u)))
+    return fail(RA_ERR_INVALID_ARG, "visit log entries must be 16-byte aligned and the count word 4-byte aligned");
+  std::lock_guard<std::mutex> lk(g_log_mu);
+  if (entries)
+    g_log = VisitLog{reinterpret_cast<uint4*>(entries), count, (unsigned long long)capacity};
+  else
+    g_log = VisitLog{nullptr, nullptr, 0};
+  return RA_OK;
+}
 
 int ra_kernel_timing(int enable) {
   KernelTimer& t = ktimer();
@@ -473,6 +496,7 @@ int ra_block_fwd(const void* q, const void* k_blk, const void* v_blk, ra_dtype d
   a.o_acc = o_acc; a.m_acc = m_acc; a.l_acc = l_acc;
   a.status = st;
   a.wait_limit_ns = wait_limit_ns();
+  a.log = visit_log();
   const int nqt = (s.Nq + 127) / 128;
   a.num_units = s.B * s.Hq * ((nqt + 1) / 2);
   TimedLaunch tl(RA_KERNEL_FWD_TC, cs);
@@ -565,6 +589,7 @@ static int ring_fwd_impl(const void* q, const void* k, const void* v, ra_dtype d
   a.o_out = o; a.o_dtype = o_dtype; a.o_bs = s.q_bs; a.lse = lse;
   a.status = st;
   a.wait_limit_ns = wait_limit_ns();
+  a.log = visit_log();
   const int T = a.ring_S / 128;
   a.num_units = s.B * s.Hq * P * ((T + 1) / 2);
   TimedLaunch tl(RA_KERNEL_FWD_TC, cs);
@@ -690,7 +715,8 @@ static int ring_bwd_impl(const void* q, const void* k, const void* v, const void
   a.scale = scale;
   a.scale_log2 = scale * 1.4426950408889634f;
   a.causal = causal;
-  a.ring_P = P; a.ring_S = s.Nq / P; a.T_m = div_magic((unsigned)(a.ring_S / 128)); a.precise = precise; a.striped = striped;
+  a.ring_P = P; a.ring_S = s.Nq / P; a.T_m = div_magic((unsigned)(a.ring_S / 128)); a.P_m = div_magic((unsigned)P);
+  a.precise = precise; a.striped = striped;
   a.host_len = host_len;
   if (host_len) {  // padded key rows: dK = dV = 0 (the kernel skips wholly padded key tiles)
     cudaError_t fe = launch_fill_padding(dk, grad_dtype, s.kv_bs, s.B, s.Nkv, s.Hkv, s.d, P, host_len, nullptr, cs);
@@ -702,6 +728,7 @@ static int ring_bwd_impl(const void* q, const void* k, const void* v, const void
   a.dk = dk; a.dv = dv; a.grad_dtype = grad_dtype; a.kv_bs = s.kv_bs;
   a.status = st;
   a.wait_limit_ns = wait_limit_ns();
+  a.log = visit_log();
   a.num_units = s.B * s.Hkv * (s.Nkv / 128);
   {
     TimedLaunch tl(RA_KERNEL_BWD_TC, cs);
@@ -1097,34 +1124,48 @@ int ra_ring_step_host(const void* q, const void* k, const void* v, const void* d
   cudaError_t e;
   // dO travels on the input side stream while q, k, v go up and the forward runs
   if ((e = cudaEventRecord(ev.e[0], main_st)) != cudaSuccess ||
-      (e = cudaStreamWaitEvent(in_st, ev.e[0], 0)) != cudaSuccess ||
-      (e = copy_batches(ws + w.dO, qel, dO, s.q_bs, s.B, qel, es, in_st)) != cudaSuccess ||
-      (e = cudaEventRecord(ev.e[1], in_st)) != cudaSuccess)
+      (e = cudaStreamWaitEvent(in_st, ev.e[0], 0)) != cudaSuccess)
     return cuda_fail(e, "dO upload");
-  if ((e = copy_batches(ws + w.q, qel, q, s.q_bs, s.B, qel, es, main_st)) != cudaSuccess ||
-      (e = copy_batches(ws + w.k, kvel, k, s.kv_bs, s.B, kvel, es, main_st)) != cudaSuccess ||
-      (e = copy_batches(ws + w.v, kvel, v, s.kv_bs, s.B, kvel, es, main_st)) != cudaSuccess)
-    return cuda_fail(e, "q, k, v upload");
+  {
+    TimedLaunch tl(RA_COPY_H2D, in_st);
+    if ((e = copy_batches(ws + w.dO, qel, dO, s.q_bs, s.B, qel, es, in_st)) != cudaSuccess)
+      return cuda_fail(e, "dO upload");
+  }
+  if ((e = cudaEventRecord(ev.e[1], in_st)) != cudaSuccess) return cuda_fail(e, "dO upload");
+  {
+    TimedLaunch tl(RA_COPY_H2D, main_st);
+    if ((e = copy_batches(ws + w.q, qel, q, s.q_bs, s.B, qel, es, main_st)) != cudaSuccess ||
+        (e = copy_batches(ws + w.k, kvel, k, s.kv_bs, s.B, kvel, es, main_st)) != cudaSuccess ||
+        (e = copy_batches(ws + w.v, kvel, v, s.kv_bs, s.B, kvel, es, main_st)) != cudaSuccess)
+      return cuda_fail(e, "q, k, v upload");
+  }
   rc = ring_fwd_impl(ws + w.q, ws + w.k, ws + w.v, dtype, packed, P, flags, scale, ws + w.o, o_dtype,
                      reinterpret_cast<float*>(ws + w.lse), ws + w.fwd, w.bwd - w.fwd, stream, nullptr);
   if (rc) return rc;
   // O and LSE travel down on the output side stream while the backward runs
   if ((e = cudaEventRecord(ev.e[2], main_st)) != cudaSuccess ||
-      (e = cudaStreamWaitEvent(out_st, ev.e[2], 0)) != cudaSuccess ||
-      (e = copy_batches(o, s.q_bs, ws + w.o, qel, s.B, qel, dtype_size(o_dtype), out_st)) != cudaSuccess ||
-      (e = cudaMemcpyAsync(lse, ws + w.lse, (size_t)s.B * s.Hq * s.Nq * 4, cudaMemcpyDefault, out_st)) !=
-          cudaSuccess ||
-      (e = cudaEventRecord(ev.e[3], out_st)) != cudaSuccess)
+      (e = cudaStreamWaitEvent(out_st, ev.e[2], 0)) != cudaSuccess)
     return cuda_fail(e, "O, LSE download");
+  {
+    TimedLaunch tl(RA_COPY_D2H, out_st);
+    if ((e = copy_batches(o, s.q_bs, ws + w.o, qel, s.B, qel, dtype_size(o_dtype), out_st)) != cudaSuccess ||
+        (e = cudaMemcpyAsync(lse, ws + w.lse, (size_t)s.B * s.Hq * s.Nq * 4, cudaMemcpyDefault, out_st)) !=
+            cudaSuccess)
+      return cuda_fail(e, "O, LSE download");
+  }
+  if ((e = cudaEventRecord(ev.e[3], out_st)) != cudaSuccess) return cuda_fail(e, "O, LSE download");
   if ((e = cudaStreamWaitEvent(main_st, ev.e[1], 0)) != cudaSuccess) return cuda_fail(e, "join dO upload");
   rc = ring_bwd_impl(ws + w.q, ws + w.k, ws + w.v, ws + w.o, o_dtype, ws + w.dO,
                      reinterpret_cast<const float*>(ws + w.lse), dtype, packed, P, flags, scale, ws + w.dq,
                      ws + w.dk, ws + w.dv, grad_dtype, ws + w.bwd, w.total - w.bwd, stream, nullptr);
   if (rc) return rc;
-  if ((e = copy_batches(dq, s.q_bs, ws + w.dq, qel, s.B, qel, gs, main_st)) != cudaSuccess ||
-      (e = copy_batches(dk, s.kv_bs, ws + w.dk, kvel, s.B, kvel, gs, main_st)) != cudaSuccess ||
-      (e = copy_batches(dv, s.kv_bs, ws + w.dv, kvel, s.B, kvel, gs, main_st)) != cudaSuccess)
-    return cuda_fail(e, "gradient download");
+  {
+    TimedLaunch tl(RA_COPY_D2H, main_st);
+    if ((e = copy_batches(dq, s.q_bs, ws + w.dq, qel, s.B, qel, gs, main_st)) != cudaSuccess ||
+        (e = copy_batches(dk, s.kv_bs, ws + w.dk, kvel, s.B, kvel, gs, main_st)) != cudaSuccess ||
+        (e = copy_batches(dv, s.kv_bs, ws + w.dv, kvel, s.B, kvel, gs, main_st)) != cudaSuccess)
+      return cuda_fail(e, "gradient download");
+  }
   if ((e = cudaStreamWaitEvent(main_st, ev.e[3], 0)) != cudaSuccess) return cuda_fail(e, "join O download");
   return RA_OK;
 }

@@ -80,7 +80,7 @@ struct BwdUnit {
   int count;  // query tiles per head
   int n_iter; // count * group
   int host, tk, per_block;  // striped layouts: key host, local key tile, query tiles per block
-  unsigned long long count_m, pb_m;  // div_magic(count), div_magic(per_block)
+  unsigned long long count_m;  // div_magic(count)
 };
 
 // Units are ordered head-major: every resident CTA works on the same
@@ -121,7 +121,6 @@ __device__ __forceinline__ BwdUnit bwd_unit(const TcBwdArgs& a, int u) {
     r.count = a.ring_P * r.per_block;
     r.n_iter = r.count * (a.Hq / a.Hkv);
     r.count_m = div_magic((unsigned)r.count);
-    r.pb_m = div_magic((unsigned)r.per_block);
     return r;
   }
   r.count = a.causal ? nT - r.jt : nT;
@@ -144,11 +143,17 @@ __device__ __forceinline__ void bwd_iter(const TcBwdArgs& a, const BwdUnit& u, i
   const int group = a.Hq / a.Hkv;
   const int hh = div_by(it, u.count_m), k = it - hh * u.count;
   *h = u.g * group + hh;
-  if (STRIPED) {  // query hosts (j + s) mod P, local tiles tk..T-1 in each
-    const int s = div_by(k, u.pb_m);
-    int qh = u.host + s;  // both < P
+  if (STRIPED) {
+    // The key tile goes round the ring once per local query tile it meets:
+    // lap t takes local query tile tk + t of hosts (j + s) mod P, s = 0..P-1.
+    // The CTAs holding the same local key tile of different hosts then read
+    // the same P query tiles within P iterations of each other, which keeps
+    // those tiles (and their dQ lines) in L2; a host-by-host sweep spreads a
+    // tile's readers over the whole unit.  Only rounding depends on the order.
+    const int lap = div_by(k, a.P_m);
+    int qh = u.host + (k - lap * a.ring_P);  // both < P
     if (qh >= a.ring_P) qh -= a.ring_P;
-    *qt = qh * (a.ring_S / 128) + u.tk + (k - s * u.per_block);
+    *qt = qh * (a.ring_S / 128) + u.tk + lap;
     return;
   }
   if (a.causal) {
@@ -302,6 +307,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
           int h, qt;
           bwd_iter<STRIPED>(a, bu, it, &h, &qt);
           if (VARLEN && !q_tile_valid<VARLEN>(a, qt)) continue;
+          if (a.log.entries) log_visit(a.log, 1u, bu.b * a.Hq + h, qt, bu.jt);
           const int s = qd_cnt & 1;
           const uint32_t par = ((qd_cnt >> 1) & 1) ^ 1;
           if (!mbar_wait(bar_q_empty(s), par, abort_flag, a.status, lim)) { ok = false; break; }

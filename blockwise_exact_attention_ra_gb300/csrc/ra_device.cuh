@@ -36,6 +36,15 @@ __device__ __forceinline__ uint32_t warp_id() {
   return __shfl_sync(0xffffffffu, threadIdx.x >> 5, 0);
 }
 
+// Appends {kind, head, query tile, key tile} to a debug visit log (one
+// thread; its entries keep their order because its atomics on one address
+// are ordered).
+__device__ __forceinline__ void log_visit(const VisitLog& log, unsigned kind, unsigned head, unsigned qt,
+                                          unsigned kt) {
+  const unsigned i = atomicAdd(log.count, 1u);
+  if (i < log.capacity) log.entries[i] = make_uint4(kind, head, qt, kt);
+}
+
 // ---------------------------------------------------------------------------
 // mbarrier
 // ---------------------------------------------------------------------------

@@ -229,8 +229,9 @@ __device__ __forceinline__ UnitInfo unit_info(const TcFwdArgs& a, int u) {
       // filled with O = 0, LSE = -inf beforehand)
       const int qlen = host_len_at(a.host_len, host, a.ring_S);
       const int la = lp * 256;
-      if (la >= qlen) r.n_iter = 0;
-      if (la + 128 >= qlen && r.has_b) {
+      if (la >= qlen) {
+        r.n_iter = 0;  // both tiles padding: the whole unit is skipped
+      } else if (la + 128 >= qlen && r.has_b) {
         r.has_b = 0;
         r.start[1] = r.n_iter;
         if (a.causal) {  // tile A leads
@@ -349,6 +350,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
           if (VARLEN && !iter_valid(ui, it, a)) continue;
           int tk = 0, blk = 0;
           const int kt = kt_at(ui, it, &tk, &blk);
+          if (a.log.entries) log_visit(a.log, 0u, ui.b * a.Hq + ui.h, ui.qa_row0 / 128, kt);
 #pragma unroll
           for (int kv = 0; kv < 2; ++kv) {  // K then V
             const int s = L_cnt % kStages;

@@ -109,6 +109,15 @@ cudaError_t launch_fill_padding(void* t, int dtype, long long bs, int B, int N, 
 cudaError_t launch_selftest_timeout(unsigned int timeout_us, int* status,
                                     cudaStream_t st);
 
+// Debug record of the tiles the tensor-core kernels bring in (see
+// ra_debug_visit_log in ra.h): entries of four uint32, appended through an
+// atomic cursor; entries past `capacity` are counted but not stored.
+struct VisitLog {
+  uint4* entries;
+  unsigned int* count;
+  unsigned long long capacity;
+};
+
 // ---------------------------------------------------------------------------
 // tcgen05 tensor-core path (d = 64 or 128, fp16/bf16 operands)
 // ---------------------------------------------------------------------------
@@ -138,6 +147,7 @@ struct TcFwdArgs {
   int* status;
   unsigned long long wait_limit_ns;
   int num_units;    // work units (pairs of 128-row query tiles)
+  VisitLog log;     // debug record of the key/value tiles loaded (off when log.entries is NULL)
 };
 cudaError_t launch_tc_fwd(TcFwdArgs& a, int num_sms, cudaStream_t st);
 
@@ -154,6 +164,7 @@ struct TcBwdArgs {
   int precise;  // two-term fp16 dS in the dK product
   int ring_P, ring_S;
   unsigned long long T_m;  // div_magic(ring_S / 128)
+  unsigned long long P_m;  // div_magic(ring_P)
   int striped;  // causal, rows in striped order (position l*P + host)
   const int* host_len;  // optional: valid rows per host (device, P entries)
   const float* lse;   // [B, Hq, N]: -LSE * log2(e)
@@ -166,6 +177,7 @@ struct TcBwdArgs {
   int* status;
   unsigned long long wait_limit_ns;
   int num_units;
+  VisitLog log;     // debug record of the query tiles loaded (off when log.entries is NULL)
 };
 cudaError_t launch_tc_bwd(TcBwdArgs& a, int num_sms, cudaStream_t st);
 

@@ -31,13 +31,28 @@ extern "C" {
 int ra_ring_fwd_noalloc(const void* q, const void* k, const void* v, ra_dtype dtype,
                         ra_shape shape, int P, int flags, float scale, void* o,
                         ra_dtype o_dtype, float* lse, void* stream) {
-  const size_t need = ra_ring_fwd_workspace_bytes(dtype, shape, P);
-  if (need > kScratchBytes) {
+  // The extents are checked before the scratch size is formed from them, so
+  // that no product of out-of-range extents can wrap around to a small size.
+  if (shape.B < 1 || shape.N_kv < 1 || shape.Hkv < 1 || shape.d < 1 || shape.N_kv >= (1 << 30) ||
+      shape.Hkv > 4096 || shape.d > 4096)
+    return ra::set_error(RA_ERR_INVALID_ARG, "ra_ring_fwd_noalloc: key/value extents out of range");
+  // B * N_kv * Hkv * d * 2 bytes, compared without overflow: B < 2^31 and
+  // N_kv * Hkv * d * 2 < 2^55
+  const unsigned long long per_batch = (unsigned long long)shape.N_kv * shape.Hkv * shape.d * 2ull;
+  const bool too_big = dtype == RA_BF16 && (unsigned long long)shape.B > kScratchBytes / per_batch;
+  const size_t need = too_big ? 0 : ra_ring_fwd_workspace_bytes(dtype, shape, P);
+  if (too_big || need > kScratchBytes) {
     char msg[256];
-    snprintf(msg, sizeof msg,
-             "ra_ring_fwd_noalloc: this shape needs %zu bytes of scratch but the built-in buffer "
-             "holds %zu; call ra_ring_fwd with a workspace instead",
-             need, kScratchBytes);
+    if (too_big)
+      snprintf(msg, sizeof msg,
+               "ra_ring_fwd_noalloc: this shape needs more scratch than the built-in buffer holds "
+               "(%zu bytes); call ra_ring_fwd with a workspace instead",
+               kScratchBytes);
+    else
+      snprintf(msg, sizeof msg,
+               "ra_ring_fwd_noalloc: this shape needs %zu bytes of scratch but the built-in buffer "
+               "holds %zu; call ra_ring_fwd with a workspace instead",
+               need, kScratchBytes);
     return ra::set_error(RA_ERR_INVALID_ARG, msg);
   }
   int dev = 0;

@@ -49,7 +49,8 @@
  *   (and dS in the backward pass) are rounded to fp16 for the second
  *   product, and bf16 operands of those products are copied to fp16 in the
  *   workspace first (exact for |x| in [2^-14, 65504]; larger values set
- *   RA_ERR_RANGE in the status word).
+ *   RA_ERR_RANGE in the status word; smaller ones become fp16 subnormals,
+ *   rounded to a multiple of 2^-24 without any status error).
  * Requirements.  Pointers 16-byte aligned; for ra_ring_fwd / ra_ring_bwd on
  *   tensor cores the host block N/P is a multiple of 128 rows; violations
  *   return RA_ERR_INVALID_ARG or RA_ERR_UNSUPPORTED.  Nothing falls back to
@@ -83,8 +84,11 @@ typedef enum { RA_F32 = 0, RA_BF16 = 1, RA_F16 = 2 } ra_dtype;
  *             "How Does This Compare to Other Long-Context Methods?").  The
  *             ring order is unchanged; every host visits every block, and in a
  *             (query host i, key host j) pair local key row lk is visible to
- *             local query row lq iff lk < lq, or lk == lq and j <= i.  Ignored
- *             without RA_CAUSAL. */
+ *             local query row lq iff lk < lq, or lk == lq and j <= i.  In the
+ *             backward pass a key tile's gradients go round the ring once per
+ *             local query tile they meet (each lap in ring order), which keeps
+ *             the query tiles that concurrent work units read in cache; only
+ *             rounding depends on that order.  Ignored without RA_CAUSAL. */
 enum { RA_CAUSAL = 1, RA_PRECISE = 2, RA_STRIPED = 4 };
 
 typedef enum {
@@ -194,6 +198,13 @@ size_t ra_ring_bwd_workspace_bytes(ra_dtype dtype, ra_dtype grad_dtype,
  *   Limit: shapes whose ra_ring_fwd_workspace_bytes() exceeds 32 MiB (the
  *   fp16 copy of V for bf16 inputs, B*N*Hkv*d*2 bytes) are rejected with
  *   RA_ERR_INVALID_ARG; fp16 and fp32 inputs need no scratch.
+ *   When the memory is taken: the array sits in a device module of its own
+ *   (no kernel shares it).  Under CUDA's lazy module loading (the default
+ *   since CUDA 12.2) a device reserves the 32 MiB at this entry point's
+ *   first call there, when its address is looked up; with eager loading
+ *   (CUDA_MODULE_LOADING=EAGER) every device the process creates a context
+ *   on reserves them as soon as the library is loaded, whether or not this
+ *   entry point is ever called.
  *   The first call on each device looks up the buffer's device address
  *   (cudaGetSymbolAddress) with that device current; make that first call
  *   before any stream capture.
@@ -301,19 +312,49 @@ const char* ra_last_error(void);
 /* Number of kernels this library has launched in this process. */
 unsigned long long ra_launch_count(void);
 
+/* Debug record of the ring schedule (off by default).  The pages debug a real
+ * ring with one log file per rank that records what each step received
+ * ("Ring Attention: Train 1M Tokens on 8GB GPUs in 2026", section "Debugging
+ * Ring Transfers with Rank-Specific Logs"); here one process runs every
+ * virtual host, and this log records, per tile the tensor-core kernels bring
+ * into shared memory, which host's work it serves:
+ *   entries  device array of `capacity` records of four uint32
+ *            {kind, head, query tile, key tile}, 16-byte aligned:
+ *            kind 0 -- the forward (ra_ring_fwd*, ra_block_fwd) loaded key/value
+ *              tile `key tile` for the unit whose first query tile is
+ *              `query tile` (128-row tiles, tensor row / 128);
+ *            kind 1 -- the backward (ra_ring_bwd*) loaded query tile
+ *              `query tile` for the unit of key/value tile `key tile`;
+ *            head = b * Hq + (query head).
+ *   count    device uint32 the kernels advance atomically (the caller zeroes
+ *            it); records past `capacity` are counted but not stored.
+ * One thread per CTA writes a unit's records, so they appear in the order the
+ * unit visits its tiles (records of different units interleave).  Tiles that
+ * are skipped (blocks in a query tile's causal future, tiles wholly in
+ * padding) leave no record.  The setting is process-wide and applies to every
+ * launch until ra_debug_visit_log(NULL, 0, NULL) turns it off; the buffers
+ * must stay valid until then.  Logging costs one atomic per tile. */
+int ra_debug_visit_log(unsigned int* entries, size_t capacity, unsigned int* count);
+
 /* Kernel timing.  While enabled, every launch of the kernels below is
  * bracketed by CUDA events recorded on the stream it is launched on;
  * ra_kernel_timing_read() waits for those events and returns the summed
  * device time (ms) and the number of launches since timing was enabled.
  * ra_kernel_timing(1) enables and resets, ra_kernel_timing(0) disables and
- * releases the events.  Used by the benchmark to time the dominant kernel. */
+ * releases the events.  Used by the benchmark to time the dominant kernel.
+ * The two copy entries time ra_ring_step_host's transfers the same way: each
+ * group of copies on one stream (q, k, v up; dO up; O and LSE down; dQ, dK,
+ * dV down) is bracketed by events on that stream, so the sums are the time
+ * the copies themselves took, whatever kernels ran beside them. */
 typedef enum {
   RA_KERNEL_FWD_TC = 0,   /* tensor-core forward (ring and block step) */
   RA_KERNEL_BWD_TC = 1,   /* tensor-core backward */
   RA_KERNEL_FWD_F32 = 2,  /* fp32 CUDA-core forward */
   RA_KERNEL_BWD_F32 = 3,  /* fp32 CUDA-core backward (both kernels) */
   RA_KERNEL_GEMM_TC = 4,  /* tensor-core GEMM of the feed-forward layer (every launch) */
-  RA_KERNEL_COUNT = 5
+  RA_COPY_H2D = 5,        /* ra_ring_step_host uploads (two groups per call) */
+  RA_COPY_D2H = 6,        /* ra_ring_step_host downloads (two groups per call) */
+  RA_KERNEL_COUNT = 7
 } ra_kernel_id;
 int ra_kernel_timing(int enable);
 int ra_kernel_timing_read(int kernel, double* total_ms, unsigned long long* launches);

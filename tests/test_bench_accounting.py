@@ -1,6 +1,8 @@
 """bench.py accounting: the per-row flops used for the CPU baseline add up to
 the whole-problem formula used for the GPU metric, and the formula matches the
 stated causal-adjusted counts (fwd 4*B*H*N^2*d/2, bwd 2.5x fwd)."""
+import os
+
 import pytest
 
 import bench
@@ -74,3 +76,24 @@ def test_reference_arm_named_workload_preset():
     c = lines[0]["config"]
     assert c["N"] == 512 and c["Hq"] == 2 and c["d"] == 64 and c["P"] == 4 and c["causal"] is False
     assert c["workload"].startswith("workload 1")
+
+
+def test_reference_arm_config_has_the_gpu_arms_keys():
+    lines = _run_bench(["--impl", "reference", "--steps", "1", "--warmup", "3", "--ref-rows", "8",
+                        "--N", "2048", "--heads", "2"])
+    assert set(lines[0]["config"]) == set(bench.bench_config(1))
+    assert lines[0]["config"]["parallelism"] == "single GPU"
+
+
+def test_input_generators_do_not_map_the_library():
+    # the reference arm and the oracle's callers import the seeded generators;
+    # that import must leave the product library unloaded
+    import subprocess
+    import sys
+    code = ("import blockwise_exact_attention_ra_gb300.inputs, oracle\n"
+            "maps = open('/proc/self/maps').read()\n"
+            "print('libra.so' in maps)\n")
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    r = subprocess.run([sys.executable, "-c", code], cwd=root, capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0, r.stderr[-2000:]
+    assert r.stdout.strip() == "False"

@@ -155,3 +155,15 @@ def test_rejected_flag_combinations(ra):
 
 def test_launch_counter_is_readable(ra):
     assert isinstance(ra.ra_launch_count(), int) and ra.ra_launch_count() >= 0
+
+
+def test_visit_log_arguments_are_checked(ra):
+    lib = ra.lib
+    # turning the log off always succeeds; a log without a count word or with a
+    # misaligned entry array is refused before anything is recorded
+    assert lib.ra_debug_visit_log(None, 0, None) == 0
+    assert lib.ra_debug_visit_log(ctypes.c_void_p(4096), 16, None) == 1
+    assert lib.ra_debug_visit_log(ctypes.c_void_p(4096), 0, ctypes.c_void_p(8192)) == 1
+    assert lib.ra_debug_visit_log(ctypes.c_void_p(4104), 16, ctypes.c_void_p(8192)) == 1
+    assert "aligned" in ra.ra_last_error()
+    assert lib.ra_debug_visit_log(None, 0, None) == 0
