@@ -310,6 +310,58 @@ def run_reference(args, ws, rank):
     print(json.dumps(line), flush=True)
 
 
+def time_named_workload(ra, cid, dev, stream, steps, warmup, peaks):
+    """One of the five named workloads through ra_ring_fwd (+ ra_ring_bwd when
+    the workload has a backward), with its own seeded inputs, mask and
+    numerics (workload 4: two-term fp16 P and dS), outputs in fp32; device
+    time with CUDA events on the launching stream."""
+    from blockwise_exact_attention_ra_gb300.inputs import WORKLOADS, make_config
+    c = WORKLOADS[cid]
+    B, N, Hq, Hkv, d, P = c["B"], c["N"], c["Hq"], c["Hkv"], c["d"], c["P"]
+    causal, bwd, precise = c["causal"], c["bwd"], cid == 4
+    scale = d ** -0.5
+    q, k, v, do = make_config(cid, dev, with_do=bwd)
+    o = torch.empty(B, N, Hq, d, dtype=torch.float32, device=dev)
+    lse = torch.empty(B, Hq, N, dtype=torch.float32, device=dev)
+    sh = ra.shape_of(q, k)
+    wsf = torch.empty(max(16, ra.ra_ring_fwd_workspace_bytes(ra._dt(q), sh, P)), dtype=torch.uint8, device=dev)
+    if bwd:
+        dq = torch.empty(B, N, Hq, d, dtype=torch.float32, device=dev)
+        dk = torch.empty(B, N, Hkv, d, dtype=torch.float32, device=dev)
+        dv = torch.empty(B, N, Hkv, d, dtype=torch.float32, device=dev)
+        wsb = torch.empty(max(16, ra.ra_ring_bwd_workspace_bytes(ra._dt(q), ra.RA_F32, sh, P)), dtype=torch.uint8,
+                          device=dev)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(3 * steps)]
+    for s_ in range(warmup + steps):
+        t = s_ - warmup
+        if t >= 0:
+            ev[3 * t].record(stream)
+        ra.ra_ring_fwd(q, k, v, P, causal, scale, o, lse, wsf, stream, precise=precise)
+        if t >= 0:
+            ev[3 * t + 1].record(stream)
+        if bwd:
+            ra.ra_ring_bwd(q, k, v, o, do, lse, P, causal, scale, dq, dk, dv, wsb, stream, precise=precise)
+        if t >= 0:
+            ev[3 * t + 2].record(stream)
+    torch.cuda.synchronize(dev)
+    ra.ra_sync_status(stream)
+    f_ms = sum(ev[3 * i].elapsed_time(ev[3 * i + 1]) for i in range(steps)) / steps
+    b_ms = sum(ev[3 * i + 1].elapsed_time(ev[3 * i + 2]) for i in range(steps)) / steps
+    ffl, bfl = algo_flops(B, N, Hq, d, causal)
+    if not bwd:
+        bfl = 0.0
+    res = {"workload": c["name"] + (" (forward)" if not bwd else " (fwd+bwd)")
+           + (", two-term fp16 P and dS" if precise else ""),
+           "steps": steps, "warmup": warmup, "ms_per_step": f_ms + b_ms,
+           "tflops": (ffl + bfl) / ((f_ms + b_ms) * 1e-3) / 1e12,
+           "fwd_ms": f_ms, "fwd_tflops": ffl / (f_ms * 1e-3) / 1e12}
+    if bwd:
+        res.update(bwd_ms=b_ms, bwd_tflops=bfl / (b_ms * 1e-3) / 1e12)
+    if c["dtype"] != torch.float32:
+        res["frac_of_peak"] = res["tflops"] / peaks["sustained"]
+    return res
+
+
 def run_ours(args, ws, rank, local):
     import blockwise_exact_attention_ra_gb300 as ra
     from blockwise_exact_attention_ra_gb300.inputs import make_tensors
@@ -606,6 +658,20 @@ def run_ours(args, ws, rank, local):
                "sample": f"{n_rows} seeded query rows of one head, fwd+bwd incl. their dK/dV "
                          f"contributions, fp64 numpy; {dt:.1f} s"}
 
+    # the other named workloads, each with its own inputs, mask and numerics,
+    # timed the same way with a few steps (1M tokens: one step of ~30 s)
+    others = None
+    if ws == 1 and not args.no_workloads and not WORKLOAD_OVERRIDDEN:
+        del q, k, v, do, o, lse, dq, dk, dv, wsf, wsb
+        torch.cuda.empty_cache()
+        others = {}
+        for cid, (st_, wu_) in {1: (10, 3), 2: (5, 3), 4: (2, 1), 5: (1, 1)}.items():
+            try:
+                others[str(cid)] = time_named_workload(ra, cid, dev, stream, st_, wu_, peaks)
+            except Exception as exc:  # one workload's failure must not lose the line
+                others[str(cid)] = {"error": f"{type(exc).__name__}: {exc}"[:300]}
+            torch.cuda.empty_cache()
+
     if rank == 0:
         line = {
             "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": ws, "steps": args.steps,
@@ -616,6 +682,7 @@ def run_ours(args, ws, rank, local):
             "fwd_ms": fwd_ms, "bwd_ms": bwd_ms,
             "fwd_tflops": fwd_fl / (fwd_ms * 1e-3) / 1e12, "bwd_tflops": bwd_fl / (bwd_ms * 1e-3) / 1e12,
             "kernels": kern, "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "striped": striped, "varlen": varlen, "ffn": ffn,
+            "other_workloads": others,
             "gpu_launches": launches, "clocks": clk,
         }
         print(json.dumps(line), flush=True)
@@ -634,6 +701,8 @@ def main():
     ap.add_argument("--no-striped", action="store_true", help="skip the striped-layout measurement")
     ap.add_argument("--no-varlen", action="store_true", help="skip the variable-length measurement")
     ap.add_argument("--no-ffn", action="store_true", help="skip the blockwise feed-forward measurement")
+    ap.add_argument("--no-workloads", action="store_true",
+                    help="skip the other named workloads (1, 2, 4, 5; the 1M-token one holds ~165 GB for ~1 min)")
     ap.add_argument("--cpu-rows", type=int, default=3072)
     ap.add_argument("--ref-rows", type=int, default=1024)
     ap.add_argument("--config", type=int, choices=[1, 2, 3, 4, 5], default=None,

@@ -39,3 +39,9 @@ def test_bench_line_has_the_contract_keys():
     # per step: 1 forward, 1 backward and the small passes around them
     assert d["gpu_launches"] >= 2 * d["steps"]
     assert d["clocks"]["sm_max_mhz"] > 0
+    # which of copies and kernels sets the end-to-end pace, from the library's own events
+    br = e["breakdown"]
+    assert br["bound_by"] in ("copies", "kernels")
+    assert br["h2d_ms_per_step"] > 0 and br["d2h_ms_per_step"] > 0 and br["kernel_ms_per_step"] > 0
+    assert br["h2d_gbs"] > 0 and br["d2h_gbs"] > 0
+    assert d["other_workloads"] is None   # the other named workloads run only at the bench workload

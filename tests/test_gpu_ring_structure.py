@@ -83,6 +83,17 @@ def test_full_gradients_at_ring_structure(ra, N, Hq, Hkv, P, causal):
     _check_all(f"N{N} P{P}", got, _oracle(q, k, v, do, causal, scale))
 
 
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float16])
+def test_full_gradients_two_batches_head_dim_64_32_hosts(ra, dtype):
+    # two batches (batch strides), d = 64 and fp16 inputs at 32 hosts of 128 rows
+    from blockwise_exact_attention_ra_gb300.inputs import make_tensors
+    N, P = 4096, 32
+    q, k, v, do = make_tensors(2, N, 4, 2, 64, dtype, "cuda", 3050 + int(dtype == torch.float16))
+    scale = 64 ** -0.5
+    got = _run(ra, q, k, v, do, P, True, scale)
+    _check_all(f"B2 d64 {dtype} P{P}", got, _oracle(q, k, v, do, True, scale), dtype)
+
+
 def test_striped_full_gradients_32_hosts(ra):
     N, H, P = 4096, 2, 32
     q, k, v, do = _inputs(N, H, H, 3101)
