@@ -37,14 +37,19 @@
 // red.global of whole rows cost ~6000 cycles per tile in the load/store unit
 // and starved the compute warps' shared-memory traffic.)
 // TMEM (512 columns): S^T [0,128) (P^T as fp16 written back into columns
-// [0,32) and [64,96)), dP^T [128,256) (dQ_i reuses [128,128+D)),
-// dK [256,256+D), dV [256+D,256+2D).
-// MMA order per iteration: dV(i) S(i+1) dK(i) dQ(i) dP(i+1); the compute
-// warps start on S(i+1) while dK(i) and dQ(i) run.
+// [0,32) and [64,96); dS^T as fp16 into [32,64) and [96,128)), dP^T [128,256)
+// (dQ_i reuses [128,128+D)), dK [256,256+D), dV [256+D,256+2D).
+// MMA order per iteration: dV(i) dQ(i) dK(i) S(i+1) dP(i+1).  dK takes dS^T
+// from TMEM (the S^T columns that P^T leaves free), so of the five products
+// only S, dP and dQ read both operands from shared memory; S(i+1) overwrites
+// those columns after dK(i), which also leaves the next Q tile's load more
+// time; dQ(i) leaves TMEM while dK(i) and S(i+1) run, before dP(i+1) needs
+// its columns.
 // With PRECISE, dS enters the dK product as two fp16 terms (hi from shared
 // memory, lo = fp16(dS - hi) from TMEM columns of dP^T that have already been
 // read: [128+64h, 128+64h+32) for query half h), so its rounding drops from
-// 2^-12 relative to about 2^-24; dQ keeps the single fp16 term.
+// 2^-12 relative to about 2^-24; dQ keeps the single fp16 term.  That mode
+// keeps the order dV(i) S(i+1) dK(i) dQ(i) dP(i+1).
 #include <math.h>
 
 #include "ra_device.cuh"
@@ -396,12 +401,12 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
         mma_commit(BAR_DP_FULL);
         const int it0 = VARLEN ? next_valid(bu, 0) : 0;
         // Per iteration i, in this order:
-        //   P(i) stored     -> dV(i) += P^T dO_i, then S(i+1) into the same columns
-        //   dS(i) stored    -> dQ(i) = dS K, then dK(i) += dS^T Q_i (dK first with
-        //                      RA_PRECISE: its low terms sit in the dP columns)
+        //   P(i) stored     -> dV(i) += P^T dO_i
+        //   dS(i) stored    -> dQ(i) = dS K, dK(i) += dS^T Q_i (dS^T from TMEM),
+        //                      then S(i+1) over the S^T columns
         //   dQ(i) read out  -> dP(i+1) into the dP/dQ columns
-        // so the compute warps form P(i+1) while dQ(i) and dK(i) run, and dP(i+1)
-        // only waits for dQ(i) to leave TMEM.
+        // With RA_PRECISE: P(i) -> dV(i), S(i+1); dS(i) -> dK(i) (its low terms sit
+        // in the dP columns), dQ(i); dQ(i) read out -> dP(i+1).
         for (int it = it0, nx; it < bu.n_iter; it = nx) {
           nx = VARLEN ? next_valid(bu, it + 1) : it + 1;
           const uint64_t dQ_mn = dQ_mn0 + s * kStageStep, dO_mn = dO_mn0 + s * kStageStep;
@@ -415,6 +420,39 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
           for (int kk = 0; kk < 8; ++kk) {
             const uint32_t pa = T_S + (kk < 4 ? kk * 8 : 64 + (kk - 4) * 8);
             mma_ts(T_DV, pa, desc_off(dO_mn, kk * 2048), id_acc, (it > it0 || kk > 0) ? 1u : 0u);
+          }
+          if (!PRECISE) {
+            // dQ(i), then dK(i) with dS^T from TMEM (the S columns P^T leaves
+            // free: queries 0-63 at 32-63, 64-127 at 96-127), then S(i+1) over them
+            if (!wait(BAR_DS_FULL, ds_cnt & 1)) break;
+            ++ds_cnt;
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk)
+              mma_ss(T_DP, desc_off(dS_mn, kk * 2048), desc_off(dK_mn, kk * 2048), id_dq, kk > 0 ? 1u : 0u);
+            mma_commit(BAR_DQ_FULL);
+            ++dq_cnt;
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk) {
+              const uint32_t la = T_S + (kk < 4 ? 32 + kk * 8 : 96 + (kk - 4) * 8);
+              mma_ts(T_DK, la, desc_off(dQ_mn, kk * 2048), id_acc, (it > it0 || kk > 0) ? 1u : 0u);
+            }
+            mma_commit(bar_q_empty(s));  // dK was the last reader of Q_i
+            mma_commit(BAR_DS_FREE);
+            ++qd_cnt;
+            if (has_next) {
+              if (!wait(bar_q_full(s2), par2)) break;
+              mma_nt(T_S, dK_k, dQ_k0 + s2 * kStageStep);
+              mma_commit(BAR_S_FULL);
+              if (!wait(BAR_DQ_FREE, (dq_cnt - 1) & 1)) break;
+              if (!wait(bar_do_full(s2), par2)) break;
+              mma_nt(T_DP, dV_k, dO_k0 + s2 * kStageStep);
+              mma_commit(BAR_DP_FULL);
+              s = s2;
+            } else {
+              mma_commit(BAR_DKV_FULL);
+              mma_commit(BAR_KV_EMPTY);
+            }
+            continue;
           }
           if (has_next) {
             if (!wait(bar_q_full(s2), par2)) break;
@@ -588,6 +626,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
           // dP^T columns [c, c+32) of this half have been read: the lo terms go
           // to its columns [c/2, c/2+16)
           if (PRECISE) RA_TMEM_ST16(tDP + c / 2, pl);
+          else RA_TMEM_ST16(tS + 32 + c / 2, pk);  // dS^T for dK, in the S columns P^T leaves free
           // 16-byte chunks (c/8 .. c/8+3) of this row, 128-byte swizzle
 #pragma unroll
           for (int q4 = 0; q4 < 4; ++q4) {
