@@ -20,7 +20,7 @@ import threading
 import torch
 
 __all__ = [
-    "RAError", "RaShape", "lib", "shape_of",
+    "RAError", "RaShape", "lib", "shape_of", "empty_like_layout",
     "ra_acc_init", "ra_block_fwd", "ra_block_fwd_workspace_bytes", "ra_merge", "ra_finalize",
     "ra_ring_fwd", "ra_ring_fwd_workspace_bytes", "ra_ring_bwd", "ra_ring_bwd_workspace_bytes",
     "ra_ring_fwd_noalloc", "ra_ring_fwd_varlen", "ra_ring_bwd_varlen", "ra_ring_step_host",
@@ -52,7 +52,9 @@ class RAError(RuntimeError):
 class RaShape(ctypes.Structure):
     _fields_ = [("B", ctypes.c_int), ("N_q", ctypes.c_int), ("N_kv", ctypes.c_int),
                 ("Hq", ctypes.c_int), ("Hkv", ctypes.c_int), ("d", ctypes.c_int),
-                ("q_bstride", ctypes.c_longlong), ("kv_bstride", ctypes.c_longlong)]
+                ("q_bstride", ctypes.c_longlong), ("kv_bstride", ctypes.c_longlong),
+                ("q_rstride", ctypes.c_longlong), ("q_hstride", ctypes.c_longlong),
+                ("kv_rstride", ctypes.c_longlong), ("kv_hstride", ctypes.c_longlong)]
 
 
 def _load():
@@ -151,23 +153,48 @@ def _bstride(t):
     return t.stride(0)
 
 
+def _strides(t):
+    """(batch, row, head) strides of a [B, N, H, d] tensor; an axis of extent
+    1 passes 0 (the library's default), since torch leaves its stride free."""
+    return tuple(t.stride(i) if t.shape[i] > 1 else 0 for i in range(3))
+
+
 def _check_layout(t, name):
-    """Tensors are [B, N, H, d] with rows of H*d contiguous elements."""
+    """Tensors are [B, N, H, d] with d contiguous; batch, row and head strides
+    are passed to the library, which checks them."""
     if t.dim() != 4:
         raise RAError(1, f"{name} must be [B, N, H, d]")
-    B, N, H, d = t.shape
-    if t.stride(3) != 1 or t.stride(2) != d or t.stride(1) != H * d:
-        raise RAError(1, f"{name} must have contiguous [N, H, d] rows (strides {t.stride()})")
+    if t.stride(3) != 1 and t.shape[3] > 1:
+        raise RAError(1, f"{name} must have a contiguous last (head) dimension (strides {t.stride()})")
+
+
+def _same_layout(t, ref, name, ref_name):
+    """o, dO, dq share q's layout and v, dk, dv share k's: the library takes one
+    set of strides per group."""
+    if t is None:
+        return
+    _check_layout(t, name)
+    if tuple(t.shape) != tuple(ref.shape) or _strides(t) != _strides(ref):
+        raise RAError(1, f"{name} must have the shape and strides of {ref_name} "
+                         f"({tuple(t.shape)} {t.stride()} vs {tuple(ref.shape)} {ref.stride()})")
 
 
 def shape_of(q, k):
-    """RaShape for q [B, Nq, Hq, d] and k [B, Nkv, Hkv, d] (batch strides taken
-    from the tensors)."""
+    """RaShape for q [B, Nq, Hq, d] and k [B, Nkv, Hkv, d], with the batch,
+    row and head strides of the tensors."""
     _check_layout(q, "q")
     _check_layout(k, "k")
     B, Nq, Hq, d = q.shape
     _, Nkv, Hkv, _ = k.shape
-    return RaShape(B, Nq, Nkv, Hq, Hkv, d, _bstride(q), _bstride(k))
+    qb, qr, qh = _strides(q)
+    kb, kr, kh = _strides(k)
+    return RaShape(B, Nq, Nkv, Hq, Hkv, d, qb, kb, qr, qh, kr, kh)
+
+
+def empty_like_layout(t, dtype=None):
+    """A new tensor with t's shape and strides (outputs of a group must share
+    its layout)."""
+    return torch.empty_strided(tuple(t.shape), t.stride(), dtype=dtype or t.dtype, device=t.device)
 
 
 RA_KERNEL_FWD_TC, RA_KERNEL_BWD_TC, RA_KERNEL_FWD_F32, RA_KERNEL_BWD_F32, RA_KERNEL_GEMM_TC = 0, 1, 2, 3, 4
@@ -235,13 +262,31 @@ def ra_finalize(o_acc, m_acc, l_acc, o_out, lse, shape, stream=None):
                            _ptr(lse), shape, _stream(stream)))
 
 
+def _fwd_shape(q, k, v, o, lse):
+    shape = shape_of(q, k)
+    _same_layout(v, k, "v", "k")
+    _same_layout(o, q, "o", "q")
+    if lse is not None and not lse.is_contiguous():
+        raise RAError(1, "lse must be packed [B, Hq, N]")
+    return shape
+
+
+def _bwd_shape(q, k, v, o, dO, lse, dq, dk, dv):
+    shape = _fwd_shape(q, k, v, o, lse)
+    for t, name in ((dO, "dO"), (dq, "dq")):
+        _same_layout(t, q, name, "q")
+    for t, name in ((dk, "dk"), (dv, "dv")):
+        _same_layout(t, k, name, "k")
+    return shape
+
+
 def ra_ring_fwd_workspace_bytes(dtype, shape, P):
     return int(_lib().ra_ring_fwd_workspace_bytes(dtype, shape, P))
 
 
 def ra_ring_fwd(q, k, v, P, causal, scale, o, lse, workspace=None, stream=None, precise=False,
                 striped=False):
-    shape = shape_of(q, k)
+    shape = _fwd_shape(q, k, v, o, lse)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _check(_lib().ra_ring_fwd(_ptr(q), _ptr(k), _ptr(v), _dt(q), shape, int(P), _flags(causal, precise, striped),
                            float(scale), _ptr(o), _dt(o), _ptr(lse), _ptr(workspace), ws_bytes,
@@ -253,7 +298,7 @@ def ra_ring_fwd_noalloc(q, k, v, P, causal, scale, o, lse, stream=None, precise=
     memory: the library's own 32 MiB per-device scratch buffer is used instead
     (shapes needing more are rejected).  Calls that overlap on the GPU race on
     that buffer."""
-    shape = shape_of(q, k)
+    shape = _fwd_shape(q, k, v, o, lse)
     _check(_lib().ra_ring_fwd_noalloc(_ptr(q), _ptr(k), _ptr(v), _dt(q), shape, int(P),
                                    _flags(causal, precise, striped), float(scale), _ptr(o), _dt(o),
                                    _ptr(lse), _stream(stream)))
@@ -263,7 +308,7 @@ def ra_ring_fwd_varlen(q, k, v, P, host_len, causal, scale, o, lse, workspace=No
                        precise=False):
     """Ring forward where host i's first host_len[i] rows are valid (host_len:
     int32 device tensor of P entries) and the rest is padding."""
-    shape = shape_of(q, k)
+    shape = _fwd_shape(q, k, v, o, lse)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _check(_lib().ra_ring_fwd_varlen(_ptr(q), _ptr(k), _ptr(v), _dt(q), shape, int(P), _ptr(host_len),
                                   _flags(causal, precise), float(scale), _ptr(o), _dt(o), _ptr(lse),
@@ -272,7 +317,7 @@ def ra_ring_fwd_varlen(q, k, v, P, host_len, causal, scale, o, lse, workspace=No
 
 def ra_ring_bwd_varlen(q, k, v, o, dO, lse, P, host_len, causal, scale, dq, dk, dv, workspace,
                        stream=None, precise=False):
-    shape = shape_of(q, k)
+    shape = _bwd_shape(q, k, v, o, dO, lse, dq, dk, dv)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _check(_lib().ra_ring_bwd_varlen(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _dt(o), _ptr(dO), _ptr(lse),
                                   _dt(q), shape, int(P), _ptr(host_len), _flags(causal, precise),
@@ -293,14 +338,9 @@ def ra_ring_step_host(q, k, v, dO, P, causal, scale, o, lse, dq, dk, dv, workspa
     for t in (q, k, v, dO, o, lse, dq, dk, dv):
         if t.is_cuda:
             raise RAError(1, "ra_ring_step_host takes host tensors")
-    # one batch stride per group: q's for dO, o, dq; k's for v, dk, dv
-    for t, ref in ((dO, q), (o, q), (dq, q), (v, k), (dk, k), (dv, k)):
-        _check_layout(t, "a host tensor")
-        if t.shape != ref.shape or (t.dim() == 4 and _bstride(t) != _bstride(ref)):
-            raise RAError(1, "ra_ring_step_host: a tensor's shape or batch stride differs from its group's")
-    if not lse.is_contiguous():
-        raise RAError(1, "ra_ring_step_host: lse must be packed [B, Hq, N]")
-    shape = shape_of(q, k)
+    # one layout per group: q's for dO, o, dq; k's for v, dk, dv (the library
+    # takes host tensors with packed rows and any batch stride)
+    shape = _bwd_shape(q, k, v, o, dO, lse, dq, dk, dv)
     ws_bytes = workspace.numel() * workspace.element_size()
     _check(_lib().ra_ring_step_host(_ptr(q), _ptr(k), _ptr(v), _ptr(dO), _dt(q), shape, int(P),
                                  _flags(causal, precise, striped), float(scale), _ptr(o), _dt(o),
@@ -368,7 +408,7 @@ def ra_ring_bwd_workspace_bytes(dtype, grad_dtype, shape, P):
 
 def ra_ring_bwd(q, k, v, o, dO, lse, P, causal, scale, dq, dk, dv, workspace, stream=None,
                 precise=False, striped=False):
-    shape = shape_of(q, k)
+    shape = _bwd_shape(q, k, v, o, dO, lse, dq, dk, dv)
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _check(_lib().ra_ring_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _dt(o), _ptr(dO), _ptr(lse),
                            _dt(q), shape, int(P), _flags(causal, precise, striped), float(scale), _ptr(dq),
@@ -390,7 +430,7 @@ def ring_attention_fwd(q, k, v, P, causal=True, scale=None, o_dtype=torch.float3
     if scale is None:
         scale = q.shape[-1] ** -0.5
     B, N, Hq, d = q.shape
-    o = torch.empty(B, N, Hq, d, dtype=o_dtype, device=q.device)
+    o = empty_like_layout(q, o_dtype)  # the q group's layout
     lse = torch.empty(B, Hq, N, dtype=torch.float32, device=q.device)
     ws = _workspace(ra_ring_fwd_workspace_bytes(_dt(q), shape_of(q, k), P), q.device)
     if host_len is not None:
@@ -408,9 +448,9 @@ def ring_attention_bwd(q, k, v, o, lse, dO, P, causal=True, scale=None,
     """Allocate dQ, dK, dV (grad_dtype) and workspace and run the ring backward."""
     if scale is None:
         scale = q.shape[-1] ** -0.5
-    dq = torch.empty(q.shape, dtype=grad_dtype, device=q.device)
-    dk = torch.empty(k.shape, dtype=grad_dtype, device=q.device)
-    dv = torch.empty(v.shape, dtype=grad_dtype, device=q.device)
+    dq = empty_like_layout(q, grad_dtype)
+    dk = empty_like_layout(k, grad_dtype)
+    dv = empty_like_layout(k, grad_dtype)
     ws = _workspace(ra_ring_bwd_workspace_bytes(_dt(q), _DTYPES[grad_dtype], shape_of(q, k), P),
                     q.device)
     if host_len is not None:

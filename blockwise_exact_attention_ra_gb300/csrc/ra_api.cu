@@ -127,15 +127,15 @@ int encoder(EncodeTiledFn* fn) {
   return RA_OK;
 }
 
-// [B, N, H, d] 16-bit tensor, batch stride bs (elements): dims (d, H, N, B),
+// [B, N, H, d] 16-bit tensor with layout L (elements): dims (d, H, N, B),
 // box (64, 1, 128, 1), 128-byte swizzle; rows past N read as zeros.
 int make_map(CUtensorMap* m, const void* base, int is_bf16, int B, int N, int H, int d,
-             long long bs) {
+             const Lay& L) {
   EncodeTiledFn fn;
   int rc = encoder(&fn);
   if (rc) return rc;
   cuuint64_t dims[4] = {(cuuint64_t)d, (cuuint64_t)H, (cuuint64_t)N, (cuuint64_t)B};
-  cuuint64_t strides[3] = {(cuuint64_t)d * 2, (cuuint64_t)H * d * 2, (cuuint64_t)bs * 2};
+  cuuint64_t strides[3] = {(cuuint64_t)L.hs * 2, (cuuint64_t)L.rs * 2, (cuuint64_t)L.bs * 2};
   cuuint32_t box[4] = {64, 1, 128, 1};
   cuuint32_t estr[4] = {1, 1, 1, 1};
   CUresult r = fn(m, is_bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4,
@@ -193,8 +193,34 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 struct Shape {
   int B, Nq, Nkv, Hq, Hkv, d;
-  long long q_bs, kv_bs;
+  Lay ql, kvl;  // q, o, dO, dq; k, v, dk, dv
 };
+
+// The layout of one group: zero strides take their packed defaults; rows of
+// d elements at n * rs + h * hs must not overlap (the smaller of the two
+// strides steps past a row, the larger past the whole inner axis), nor may
+// one batch overlap the next.
+int group_layout(const char* name, int N, int H, int d, long long bs, long long rs, long long hs, Lay* out) {
+  if (bs < 0 || rs < 0 || hs < 0) return fail(RA_ERR_INVALID_ARG, "%s strides must be >= 0", name);
+  if (rs == 0) rs = (long long)H * d;
+  if (hs == 0) hs = d;
+  long long s1 = rs, n1 = N, s2 = hs, n2 = H;
+  if (s1 > s2) {
+    long long t = s1; s1 = s2; s2 = t;
+    t = n1; n1 = n2; n2 = t;
+  }
+  const long long inner = (n1 - 1) * s1 + d;
+  if ((n1 > 1 && s1 < d) || (n2 > 1 && s2 < inner))
+    return fail(RA_ERR_INVALID_ARG, "%s row and head strides (%lld, %lld) make rows of %d elements overlap", name,
+                rs, hs, d);
+  const long long extent = (long long)(N - 1) * rs + (long long)(H - 1) * hs + d;
+  if (bs == 0) bs = extent;
+  if (bs < extent)
+    return fail(RA_ERR_INVALID_ARG, "%s batch stride %lld is smaller than one batch (%lld elements)", name, bs,
+                extent);
+  *out = Lay{bs, rs, hs};
+  return RA_OK;
+}
 
 int check_shape(const ra_shape& s, Shape* out) {
   if (s.B < 1 || s.N_q < 1 || s.N_kv < 1 || s.Hq < 1 || s.Hkv < 1 || s.d < 1)
@@ -203,15 +229,21 @@ int check_shape(const ra_shape& s, Shape* out) {
   if (s.Hq % s.Hkv) return fail(RA_ERR_INVALID_ARG, "Hq=%d is not a multiple of Hkv=%d", s.Hq, s.Hkv);
   if (s.N_q >= (1 << 30) || s.N_kv >= (1 << 30) || s.Hq > 4096 || s.d > 4096)
     return fail(RA_ERR_INVALID_ARG, "shape extent too large");
-  Shape r{s.B, s.N_q, s.N_kv, s.Hq, s.Hkv, s.d, s.q_bstride, s.kv_bstride};
-  const long long qrow = (long long)s.N_q * s.Hq * s.d, kvrow = (long long)s.N_kv * s.Hkv * s.d;
-  if (r.q_bs == 0) r.q_bs = qrow;
-  if (r.kv_bs == 0) r.kv_bs = kvrow;
-  if (r.q_bs < qrow || r.kv_bs < kvrow)
-    return fail(RA_ERR_INVALID_ARG, "batch stride smaller than one batch (q %lld < %lld or kv %lld < %lld)",
-                r.q_bs, qrow, r.kv_bs, kvrow);
+  const long long big = 1ll << 50;  // keeps every offset product far from overflow
+  if (s.q_bstride > big || s.kv_bstride > big || s.q_rstride > big || s.q_hstride > big || s.kv_rstride > big ||
+      s.kv_hstride > big)
+    return fail(RA_ERR_INVALID_ARG, "stride too large");
+  Shape r{s.B, s.N_q, s.N_kv, s.Hq, s.Hkv, s.d, {}, {}};
+  int rc;
+  if ((rc = group_layout("q", s.N_q, s.Hq, s.d, s.q_bstride, s.q_rstride, s.q_hstride, &r.ql)) ||
+      (rc = group_layout("kv", s.N_kv, s.Hkv, s.d, s.kv_bstride, s.kv_rstride, s.kv_hstride, &r.kvl)))
+    return rc;
   *out = r;
   return RA_OK;
+}
+
+bool is_packed(const Lay& L, long long N, long long H, long long d) {
+  return L.rs == H * d && L.hs == d;
 }
 
 int check_ptr(const void* p, const char* name) {
@@ -230,8 +262,9 @@ int check_scale(float scale) {
 int check_tc(const Shape& s, int dtype) {
   if (s.d != 64 && s.d != 128)
     return fail(RA_ERR_UNSUPPORTED, "tensor-core path supports d in {64, 128} (got %d)", s.d);
-  if (((s.q_bs * 2) & 15) || ((s.kv_bs * 2) & 15))
-    return fail(RA_ERR_INVALID_ARG, "batch strides must be multiples of 16 bytes");
+  for (const Lay* L : {&s.ql, &s.kvl})
+    if ((L->bs % 8) || (L->rs % 8) || (L->hs % 8))
+      return fail(RA_ERR_INVALID_ARG, "16-bit tensor-core inputs need strides that are multiples of 8 elements");
   if (!device_is_sm103())
     return fail(RA_ERR_UNSUPPORTED, "tensor-core kernels are built for sm_103a only");
   (void)dtype;
@@ -424,7 +457,7 @@ int ra_finalize(const float* o_acc, const float* m_acc, const float* l_acc, void
     return rc;
   int* st;
   if ((rc = status_ptr(&st))) return rc;
-  cudaError_t e = launch_finalize(o_acc, m_acc, l_acc, o_out, o_dtype, s.q_bs, lse, s.B, s.Nq,
+  cudaError_t e = launch_finalize(o_acc, m_acc, l_acc, o_out, o_dtype, s.ql, lse, s.B, s.Nq,
                                   s.Hq, s.d, static_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? RA_OK : cuda_fail(e, "finalize launch");
 }
@@ -460,7 +493,7 @@ int ra_block_fwd(const void* q, const void* k_blk, const void* v_blk, ra_dtype d
     a.k = static_cast<const float*>(k_blk);
     a.v = static_cast<const float*>(v_blk);
     a.B = s.B; a.Nq = s.Nq; a.Nkv = s.Nkv; a.Hq = s.Hq; a.Hkv = s.Hkv; a.d = s.d;
-    a.q_bs = s.q_bs; a.kv_bs = s.kv_bs;
+    a.ql = s.ql; a.kvl = s.kvl;
     a.scale = scale; a.causal = causal; a.q_off = q_off; a.kv_off = kv_off;
     a.P = 0; a.S = 0;
     a.o_acc = o_acc; a.m_acc = m_acc; a.l_acc = l_acc;
@@ -475,18 +508,17 @@ int ra_block_fwd(const void* q, const void* k_blk, const void* v_blk, ra_dtype d
     if (!workspace || ws_bytes < need)
       return fail(RA_ERR_INVALID_ARG, "workspace of %zu bytes needed (got %zu)", need, ws_bytes);
     if ((rc = check_ptr(workspace, "workspace"))) return rc;
-    cudaError_t e = launch_to_f16(v_blk, RA_BF16, s.kv_bs, workspace, s.B,
-                                  (long long)s.Nkv * s.Hkv * s.d, st, cs);
+    cudaError_t e = launch_to_f16(v_blk, RA_BF16, s.kvl, workspace, s.B, s.Nkv, s.Hkv, s.d, st, cs);
     if (e != cudaSuccess) return cuda_fail(e, "v -> fp16 launch");
     v16 = workspace;
   }
   TcFwdArgs a;
   memset(&a, 0, sizeof a);
   const int bf = dtype == RA_BF16;
-  if ((rc = make_map(&a.tm_q, q, bf, s.B, s.Nq, s.Hq, s.d, s.q_bs))) return rc;
-  if ((rc = make_map(&a.tm_k, k_blk, bf, s.B, s.Nkv, s.Hkv, s.d, s.kv_bs))) return rc;
+  if ((rc = make_map(&a.tm_q, q, bf, s.B, s.Nq, s.Hq, s.d, s.ql))) return rc;
+  if ((rc = make_map(&a.tm_k, k_blk, bf, s.B, s.Nkv, s.Hkv, s.d, s.kvl))) return rc;
   if ((rc = make_map(&a.tm_v, v16, 0, s.B, s.Nkv, s.Hkv, s.d,
-                     dtype == RA_BF16 ? (long long)s.Nkv * s.Hkv * s.d : s.kv_bs)))
+                     dtype == RA_BF16 ? packed_lay(s.Nkv, s.Hkv, s.d) : s.kvl)))
     return rc;
   a.qk_bf16 = bf;
   a.B = s.B; a.Nq = s.Nq; a.Nkv = s.Nkv; a.Hq = s.Hq; a.Hkv = s.Hkv; a.d = s.d;
@@ -548,10 +580,10 @@ static int ring_fwd_impl(const void* q, const void* k, const void* v, ra_dtype d
     a.k = static_cast<const float*>(k);
     a.v = static_cast<const float*>(v);
     a.B = s.B; a.Nq = s.Nq; a.Nkv = s.Nkv; a.Hq = s.Hq; a.Hkv = s.Hkv; a.d = s.d;
-    a.q_bs = s.q_bs; a.kv_bs = s.kv_bs;
+    a.ql = s.ql; a.kvl = s.kvl;
     a.scale = scale; a.causal = causal;
     a.P = P; a.S = s.Nq / P; a.striped = striped; a.host_len = host_len;
-    a.o_out = o; a.o_dtype = o_dtype; a.o_bs = s.q_bs; a.lse = lse;
+    a.o_out = o; a.o_dtype = o_dtype; a.lse = lse;
     TimedLaunch tl(RA_KERNEL_FWD_F32, cs);
     cudaError_t e = launch_simt_fwd(a, cs);
     return e == cudaSuccess ? RA_OK : cuda_fail(e, "fp32 ring forward launch");
@@ -563,18 +595,17 @@ static int ring_fwd_impl(const void* q, const void* k, const void* v, ra_dtype d
     if (!workspace || ws_bytes < need)
       return fail(RA_ERR_INVALID_ARG, "workspace of %zu bytes needed (got %zu)", need, ws_bytes);
     if ((rc = check_ptr(workspace, "workspace"))) return rc;
-    cudaError_t e = launch_to_f16(v, RA_BF16, s.kv_bs, workspace, s.B,
-                                  (long long)s.Nkv * s.Hkv * s.d, st, cs);
+    cudaError_t e = launch_to_f16(v, RA_BF16, s.kvl, workspace, s.B, s.Nkv, s.Hkv, s.d, st, cs);
     if (e != cudaSuccess) return cuda_fail(e, "v -> fp16 launch");
     v16 = workspace;
   }
   TcFwdArgs a;
   memset(&a, 0, sizeof a);
   const int bf = dtype == RA_BF16;
-  if ((rc = make_map(&a.tm_q, q, bf, s.B, s.Nq, s.Hq, s.d, s.q_bs))) return rc;
-  if ((rc = make_map(&a.tm_k, k, bf, s.B, s.Nkv, s.Hkv, s.d, s.kv_bs))) return rc;
+  if ((rc = make_map(&a.tm_q, q, bf, s.B, s.Nq, s.Hq, s.d, s.ql))) return rc;
+  if ((rc = make_map(&a.tm_k, k, bf, s.B, s.Nkv, s.Hkv, s.d, s.kvl))) return rc;
   if ((rc = make_map(&a.tm_v, v16, 0, s.B, s.Nkv, s.Hkv, s.d,
-                     dtype == RA_BF16 ? (long long)s.Nkv * s.Hkv * s.d : s.kv_bs)))
+                     dtype == RA_BF16 ? packed_lay(s.Nkv, s.Hkv, s.d) : s.kvl)))
     return rc;
   a.qk_bf16 = bf;
   a.B = s.B; a.Nq = s.Nq; a.Nkv = s.Nkv; a.Hq = s.Hq; a.Hkv = s.Hkv; a.d = s.d;
@@ -583,10 +614,10 @@ static int ring_fwd_impl(const void* q, const void* k, const void* v, ra_dtype d
   a.ring_P = P; a.ring_S = s.Nq / P; a.T_m = div_magic((unsigned)(a.ring_S / 128)); a.mode = 0; a.precise = precise; a.striped = striped;
   a.host_len = host_len;
   if (host_len) {  // padded rows: O = 0, LSE = -inf (the kernel skips them)
-    cudaError_t fe = launch_fill_padding(o, o_dtype, s.q_bs, s.B, s.Nq, s.Hq, s.d, P, host_len, lse, cs);
+    cudaError_t fe = launch_fill_padding(o, o_dtype, s.ql, s.B, s.Nq, s.Hq, s.d, P, host_len, lse, cs);
     if (fe != cudaSuccess) return cuda_fail(fe, "padding fill launch");
   }
-  a.o_out = o; a.o_dtype = o_dtype; a.o_bs = s.q_bs; a.lse = lse;
+  a.o_out = o; a.o_dtype = o_dtype; a.ol = s.ql; a.lse = lse;
   a.status = st;
   a.wait_limit_ns = wait_limit_ns();
   a.log = visit_log();
@@ -662,7 +693,7 @@ static int ring_bwd_impl(const void* q, const void* k, const void* v, const void
   if (dtype == RA_F32) {
     if (s.d != 32 && s.d != 64 && s.d != 128)
       return fail(RA_ERR_UNSUPPORTED, "fp32 path supports d in {32, 64, 128} (got %d)", s.d);
-    cudaError_t e = launch_bwd_dot(dO, RA_F32, o, o_dtype, s.q_bs, Dv, nullptr, nullptr, s.B, s.Nq,
+    cudaError_t e = launch_bwd_dot(dO, RA_F32, o, o_dtype, s.ql, Dv, nullptr, nullptr, s.B, s.Nq,
                                    s.Hq, s.d, cs);
     if (e != cudaSuccess) return cuda_fail(e, "bwd D launch");
     SimtBwdArgs a{};
@@ -673,7 +704,7 @@ static int ring_bwd_impl(const void* q, const void* k, const void* v, const void
     a.lse = lse;
     a.Dvec = Dv;
     a.B = s.B; a.N = s.Nq; a.Hq = s.Hq; a.Hkv = s.Hkv; a.d = s.d;
-    a.q_bs = s.q_bs; a.kv_bs = s.kv_bs;
+    a.ql = s.ql; a.kvl = s.kvl;
     a.scale = scale; a.causal = causal;
     a.P = P; a.S = s.Nq / P; a.striped = striped; a.host_len = host_len;
     a.dq = dq; a.dk = dk; a.dv = dv; a.grad_dtype = grad_dtype;
@@ -686,18 +717,19 @@ static int ring_bwd_impl(const void* q, const void* k, const void* v, const void
   if ((rc = check_tc(s, dtype))) return rc;
   const long long qel = (long long)s.Nq * s.Hq * s.d, kvel = (long long)s.Nkv * s.Hkv * s.d;
   float* lse2 = reinterpret_cast<float*>(ws + w.lse2);
-  cudaError_t e = launch_bwd_dot(dO, dtype, o, o_dtype, s.q_bs, Dv, lse, lse2, s.B, s.Nq, s.Hq,
+  cudaError_t e = launch_bwd_dot(dO, dtype, o, o_dtype, s.ql, Dv, lse, lse2, s.B, s.Nq, s.Hq,
                                  s.d, cs);
   if (e != cudaSuccess) return cuda_fail(e, "bwd D launch");
   const void *q16 = q, *k16 = k, *v16 = v, *do16 = dO;
-  long long q16_bs = s.q_bs, kv16_bs = s.kv_bs;
+  Lay q16_l = s.ql, kv16_l = s.kvl;
   if (dtype == RA_BF16) {
     q16 = ws + w.q16; k16 = ws + w.k16; v16 = ws + w.v16; do16 = ws + w.do16;
-    q16_bs = qel; kv16_bs = kvel;
-    if ((e = launch_to_f16(q, RA_BF16, s.q_bs, ws + w.q16, s.B, qel, st, cs)) != cudaSuccess ||
-        (e = launch_to_f16(k, RA_BF16, s.kv_bs, ws + w.k16, s.B, kvel, st, cs)) != cudaSuccess ||
-        (e = launch_to_f16(v, RA_BF16, s.kv_bs, ws + w.v16, s.B, kvel, st, cs)) != cudaSuccess ||
-        (e = launch_to_f16(dO, RA_BF16, s.q_bs, ws + w.do16, s.B, qel, st, cs)) != cudaSuccess)
+    q16_l = packed_lay(s.Nq, s.Hq, s.d);
+    kv16_l = packed_lay(s.Nkv, s.Hkv, s.d);
+    if ((e = launch_to_f16(q, RA_BF16, s.ql, ws + w.q16, s.B, s.Nq, s.Hq, s.d, st, cs)) != cudaSuccess ||
+        (e = launch_to_f16(k, RA_BF16, s.kvl, ws + w.k16, s.B, s.Nkv, s.Hkv, s.d, st, cs)) != cudaSuccess ||
+        (e = launch_to_f16(v, RA_BF16, s.kvl, ws + w.v16, s.B, s.Nkv, s.Hkv, s.d, st, cs)) != cudaSuccess ||
+        (e = launch_to_f16(dO, RA_BF16, s.ql, ws + w.do16, s.B, s.Nq, s.Hq, s.d, st, cs)) != cudaSuccess)
       return cuda_fail(e, "fp16 operand copy launch");
   }
   float* dq_acc = reinterpret_cast<float*>(ws + w.dq);
@@ -705,10 +737,10 @@ static int ring_bwd_impl(const void* q, const void* k, const void* v, const void
   if (e != cudaSuccess) return cuda_fail(e, "zero dq accumulator");
   TcBwdArgs a;
   memset(&a, 0, sizeof a);
-  if ((rc = make_map(&a.tm_q, q16, 0, s.B, s.Nq, s.Hq, s.d, q16_bs)) ||
-      (rc = make_map(&a.tm_do, do16, 0, s.B, s.Nq, s.Hq, s.d, q16_bs)) ||
-      (rc = make_map(&a.tm_k, k16, 0, s.B, s.Nkv, s.Hkv, s.d, kv16_bs)) ||
-      (rc = make_map(&a.tm_v, v16, 0, s.B, s.Nkv, s.Hkv, s.d, kv16_bs)) ||
+  if ((rc = make_map(&a.tm_q, q16, 0, s.B, s.Nq, s.Hq, s.d, q16_l)) ||
+      (rc = make_map(&a.tm_do, do16, 0, s.B, s.Nq, s.Hq, s.d, q16_l)) ||
+      (rc = make_map(&a.tm_k, k16, 0, s.B, s.Nkv, s.Hkv, s.d, kv16_l)) ||
+      (rc = make_map(&a.tm_v, v16, 0, s.B, s.Nkv, s.Hkv, s.d, kv16_l)) ||
       (rc = make_map_f32(&a.tm_dq, dq_acc, s.B, s.Nq, s.Hq, s.d)))
     return rc;
   a.B = s.B; a.N = s.Nq; a.Hq = s.Hq; a.Hkv = s.Hkv; a.d = s.d;
@@ -719,13 +751,13 @@ static int ring_bwd_impl(const void* q, const void* k, const void* v, const void
   a.precise = precise; a.striped = striped;
   a.host_len = host_len;
   if (host_len) {  // padded key rows: dK = dV = 0 (the kernel skips wholly padded key tiles)
-    cudaError_t fe = launch_fill_padding(dk, grad_dtype, s.kv_bs, s.B, s.Nkv, s.Hkv, s.d, P, host_len, nullptr, cs);
+    cudaError_t fe = launch_fill_padding(dk, grad_dtype, s.kvl, s.B, s.Nkv, s.Hkv, s.d, P, host_len, nullptr, cs);
     if (fe == cudaSuccess)
-      fe = launch_fill_padding(dv, grad_dtype, s.kv_bs, s.B, s.Nkv, s.Hkv, s.d, P, host_len, nullptr, cs);
+      fe = launch_fill_padding(dv, grad_dtype, s.kvl, s.B, s.Nkv, s.Hkv, s.d, P, host_len, nullptr, cs);
     if (fe != cudaSuccess) return cuda_fail(fe, "padding fill launch");
   }
   a.lse = lse2; a.Dvec = Dv; a.dq_acc = dq_acc;
-  a.dk = dk; a.dv = dv; a.grad_dtype = grad_dtype; a.kv_bs = s.kv_bs;
+  a.dk = dk; a.dv = dv; a.grad_dtype = grad_dtype; a.kvl = s.kvl;
   a.status = st;
   a.wait_limit_ns = wait_limit_ns();
   a.log = visit_log();
@@ -735,7 +767,7 @@ static int ring_bwd_impl(const void* q, const void* k, const void* v, const void
     e = launch_tc_bwd(a, device_sms(), cs);
   }
   if (e != cudaSuccess) return cuda_fail(e, "tensor-core ring backward launch");
-  e = launch_f32_to(dq_acc, dq, grad_dtype, s.q_bs, s.B, qel, scale, cs);
+  e = launch_f32_to(dq_acc, dq, grad_dtype, s.ql, s.B, s.Nq, s.Hq, s.d, scale, cs);
   return e == cudaSuccess ? RA_OK : cuda_fail(e, "dq conversion launch");
 }
 
@@ -982,8 +1014,8 @@ HostWs host_layout(int dtype, int o_dtype, int grad_dtype, const ra_shape& sh, i
   HostWs w{};
   const size_t qel = (size_t)sh.B * sh.N_q * sh.Hq * sh.d, kvel = (size_t)sh.B * sh.N_kv * sh.Hkv * sh.d;
   ra_shape packed = sh;
-  packed.q_bstride = 0;
-  packed.kv_bstride = 0;
+  packed.q_bstride = packed.q_rstride = packed.q_hstride = 0;
+  packed.kv_bstride = packed.kv_rstride = packed.kv_hstride = 0;
   size_t off = 0;
   auto take = [&off](size_t bytes) {
     const size_t at = off;
@@ -1092,6 +1124,10 @@ int ra_ring_step_host(const void* q, const void* k, const void* v, const void* d
   for (int i = 0; i < 4; ++i)
     if (!ins[i]) return fail(RA_ERR_INVALID_ARG, "%s is NULL", in_names[i]);
   if (!o || !lse || !dq || !dk || !dv) return fail(RA_ERR_INVALID_ARG, "an output pointer is NULL");
+  if (!is_packed(s.ql, s.Nq, s.Hq, s.d) || !is_packed(s.kvl, s.Nkv, s.Hkv, s.d))
+    return fail(RA_ERR_UNSUPPORTED,
+                "ra_ring_step_host takes host tensors with packed rows (row stride H*d, head stride d); "
+                "batch strides may be any");
   const HostWs w = host_layout(dtype, o_dtype, grad_dtype, shape, P);
   if (!workspace || ws_bytes < w.total)
     return fail(RA_ERR_INVALID_ARG, "workspace of %zu bytes needed (got %zu)", w.total, ws_bytes);
@@ -1104,8 +1140,8 @@ int ra_ring_step_host(const void* q, const void* k, const void* v, const void* d
       return fail(RA_ERR_UNSUPPORTED, "fp32 path supports d in {32, 64, 128} (got %d)", s.d);
   } else {
     Shape packed = s;
-    packed.q_bs = (long long)s.Nq * s.Hq * s.d;
-    packed.kv_bs = (long long)s.Nkv * s.Hkv * s.d;
+    packed.ql = packed_lay(s.Nq, s.Hq, s.d);
+    packed.kvl = packed_lay(s.Nkv, s.Hkv, s.d);
     if ((rc = check_tc(packed, dtype))) return rc;
   }
   cudaStream_t main_st = static_cast<cudaStream_t>(stream), in_st, out_st;
@@ -1119,8 +1155,8 @@ int ra_ring_step_host(const void* q, const void* k, const void* v, const void* d
   const long long qel = (long long)s.Nq * s.Hq * s.d, kvel = (long long)s.Nkv * s.Hkv * s.d;
   const size_t es = dtype_size(dtype), gs = dtype_size(grad_dtype);
   ra_shape packed = shape;
-  packed.q_bstride = 0;
-  packed.kv_bstride = 0;
+  packed.q_bstride = packed.q_rstride = packed.q_hstride = 0;
+  packed.kv_bstride = packed.kv_rstride = packed.kv_hstride = 0;
   cudaError_t e;
   // dO travels on the input side stream while q, k, v go up and the forward runs
   if ((e = cudaEventRecord(ev.e[0], main_st)) != cudaSuccess ||
@@ -1128,15 +1164,15 @@ int ra_ring_step_host(const void* q, const void* k, const void* v, const void* d
     return cuda_fail(e, "dO upload");
   {
     TimedLaunch tl(RA_COPY_H2D, in_st);
-    if ((e = copy_batches(ws + w.dO, qel, dO, s.q_bs, s.B, qel, es, in_st)) != cudaSuccess)
+    if ((e = copy_batches(ws + w.dO, qel, dO, s.ql.bs, s.B, qel, es, in_st)) != cudaSuccess)
       return cuda_fail(e, "dO upload");
   }
   if ((e = cudaEventRecord(ev.e[1], in_st)) != cudaSuccess) return cuda_fail(e, "dO upload");
   {
     TimedLaunch tl(RA_COPY_H2D, main_st);
-    if ((e = copy_batches(ws + w.q, qel, q, s.q_bs, s.B, qel, es, main_st)) != cudaSuccess ||
-        (e = copy_batches(ws + w.k, kvel, k, s.kv_bs, s.B, kvel, es, main_st)) != cudaSuccess ||
-        (e = copy_batches(ws + w.v, kvel, v, s.kv_bs, s.B, kvel, es, main_st)) != cudaSuccess)
+    if ((e = copy_batches(ws + w.q, qel, q, s.ql.bs, s.B, qel, es, main_st)) != cudaSuccess ||
+        (e = copy_batches(ws + w.k, kvel, k, s.kvl.bs, s.B, kvel, es, main_st)) != cudaSuccess ||
+        (e = copy_batches(ws + w.v, kvel, v, s.kvl.bs, s.B, kvel, es, main_st)) != cudaSuccess)
       return cuda_fail(e, "q, k, v upload");
   }
   rc = ring_fwd_impl(ws + w.q, ws + w.k, ws + w.v, dtype, packed, P, flags, scale, ws + w.o, o_dtype,
@@ -1148,7 +1184,7 @@ int ra_ring_step_host(const void* q, const void* k, const void* v, const void* d
     return cuda_fail(e, "O, LSE download");
   {
     TimedLaunch tl(RA_COPY_D2H, out_st);
-    if ((e = copy_batches(o, s.q_bs, ws + w.o, qel, s.B, qel, dtype_size(o_dtype), out_st)) != cudaSuccess ||
+    if ((e = copy_batches(o, s.ql.bs, ws + w.o, qel, s.B, qel, dtype_size(o_dtype), out_st)) != cudaSuccess ||
         (e = cudaMemcpyAsync(lse, ws + w.lse, (size_t)s.B * s.Hq * s.Nq * 4, cudaMemcpyDefault, out_st)) !=
             cudaSuccess)
       return cuda_fail(e, "O, LSE download");
@@ -1161,9 +1197,9 @@ int ra_ring_step_host(const void* q, const void* k, const void* v, const void* d
   if (rc) return rc;
   {
     TimedLaunch tl(RA_COPY_D2H, main_st);
-    if ((e = copy_batches(dq, s.q_bs, ws + w.dq, qel, s.B, qel, gs, main_st)) != cudaSuccess ||
-        (e = copy_batches(dk, s.kv_bs, ws + w.dk, kvel, s.B, kvel, gs, main_st)) != cudaSuccess ||
-        (e = copy_batches(dv, s.kv_bs, ws + w.dv, kvel, s.B, kvel, gs, main_st)) != cudaSuccess)
+    if ((e = copy_batches(dq, s.ql.bs, ws + w.dq, qel, s.B, qel, gs, main_st)) != cudaSuccess ||
+        (e = copy_batches(dk, s.kvl.bs, ws + w.dk, kvel, s.B, kvel, gs, main_st)) != cudaSuccess ||
+        (e = copy_batches(dv, s.kvl.bs, ws + w.dv, kvel, s.B, kvel, gs, main_st)) != cudaSuccess)
       return cuda_fail(e, "gradient download");
   }
   if ((e = cudaStreamWaitEvent(main_st, ev.e[3], 0)) != cudaSuccess) return cuda_fail(e, "join O download");

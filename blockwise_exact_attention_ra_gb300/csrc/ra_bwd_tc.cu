@@ -716,7 +716,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
       if (!mbar_wait(BAR_DKV_FULL, k & 1, abort_flag, a.status, lim)) { ok = false; break; }
       tc_fence_after();
       const long long row = (long long)bu.jt * 128 + r;
-      const long long base = bu.b * a.kv_bs + (row * a.Hkv + bu.g) * D;
+      const long long base = lay_at(a.kvl, bu.b, row, bu.g);
 #pragma unroll
       for (int which = 0; which < 2; ++which) {
         const uint32_t src = (which == 0 ? T_DK : T_DV) + lane_off;

@@ -611,7 +611,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
       // epilogue
       if (a.mode == 0) {
         const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
-        const long long out = ui.b * a.o_bs + ((long long)row * a.Hq + ui.h) * D;
+        const long long out = lay_at(a.ol, ui.b, row, ui.h);
 #pragma unroll
         for (int c = 0; c < D; c += 32) {
           uint32_t ov[32];

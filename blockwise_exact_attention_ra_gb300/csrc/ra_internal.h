@@ -22,12 +22,16 @@ __host__ __device__ inline int div_by(int n, unsigned long long m) {
   return (int)(((unsigned long long)(unsigned)n * m) >> 40);
 }
 
-// Rows of a [B, N, H, d] tensor: element (b, n, h, c) sits at
-// b * bstride + (n * H + h) * d + c.
-struct Rows {
-  const void* ptr;
-  long long bstride;
+// Layout of a [B, N, H, d] tensor with d contiguous: element (b, n, h, c)
+// sits at b * bs + n * rs + h * hs + c (elements).  Packed: rs = H * d,
+// hs = d, bs = N * H * d.
+struct Lay {
+  long long bs, rs, hs;
 };
+__host__ __device__ inline long long lay_at(const Lay& L, long long b, long long n, long long h) {
+  return b * L.bs + n * L.rs + h * L.hs;
+}
+inline Lay packed_lay(long long N, long long H, long long d) { return Lay{N * H * d, H * d, d}; }
 
 // ---------------------------------------------------------------------------
 // fp32 CUDA-core path
@@ -37,7 +41,7 @@ struct SimtFwdArgs {
   const float* k;
   const float* v;
   int B, Nq, Nkv, Hq, Hkv, d;
-  long long q_bs, kv_bs;
+  Lay ql, kvl;              // q; k and v
   float scale;
   int causal;
   long long q_off, kv_off;  // block mode: global positions of row 0
@@ -47,9 +51,8 @@ struct SimtFwdArgs {
   float* o_acc;             // block mode state (read + written)
   float* m_acc;
   float* l_acc;
-  void* o_out;              // ring mode outputs
+  void* o_out;              // ring mode outputs (layout ql)
   int o_dtype;
-  long long o_bs;
   float* lse;
 };
 
@@ -61,7 +64,7 @@ struct SimtBwdArgs {
   const float* lse;
   const float* Dvec;  // [B, Hq, N]
   int B, N, Hq, Hkv, d;
-  long long q_bs, kv_bs;
+  Lay ql, kvl;        // q, dO, dq; k, v, dk, dv
   float scale;
   int causal;
   int P, S;
@@ -85,26 +88,25 @@ cudaError_t launch_merge(float* oa, float* ma, float* la, const float* ob,
                          const float* mb, const float* lb, int B, int N, int H, int d,
                          cudaStream_t st);
 cudaError_t launch_finalize(const float* o, const float* m, const float* l, void* out,
-                            int out_dtype, long long out_bs, float* lse, int B, int N,
+                            int out_dtype, Lay out_l, float* lse, int B, int N,
                             int H, int d, cudaStream_t st);
-// dst (packed fp16 [B, rows_per_batch]) <- src (dtype, batch stride src_bs);
-// values beyond the fp16 range set RA_ERR_RANGE in *status.
-cudaError_t launch_to_f16(const void* src, int src_dtype, long long src_bs, void* dst,
-                          int B, long long elems_per_batch, int* status,
-                          cudaStream_t st);
+// dst (packed fp16 [B, N, H, d]) <- src (dtype, layout src_l; rows 16-byte
+// aligned, d % 8 == 0); values beyond the fp16 range set RA_ERR_RANGE in *status.
+cudaError_t launch_to_f16(const void* src, int src_dtype, Lay src_l, void* dst,
+                          int B, int N, int H, int d, int* status, cudaStream_t st);
 // D[b, h, n] = sum_c dO[b, n, h, c] * O[b, n, h, c].  When lse2 is given (the
 // tensor-core backward) both come out negated: D[b, h, n] = -sum(...) and
 // lse2[b, h, n] = -lse[b, h, n] * log2(e), the terms that kernel adds.
 cudaError_t launch_bwd_dot(const void* dO, int do_dtype, const void* o, int o_dtype,
-                           long long q_bs, float* D, const float* lse, float* lse2, int B,
+                           Lay ql, float* D, const float* lse, float* lse2, int B,
                            int N, int H, int d, cudaStream_t st);
-// out (dtype, batch stride out_bs) <- mul * src (packed fp32)
-cudaError_t launch_f32_to(const float* src, void* out, int out_dtype, long long out_bs,
-                          int B, long long elems_per_batch, float mul, cudaStream_t st);
+// out (dtype, layout out_l) <- mul * src (packed fp32 [B, N, H, d])
+cudaError_t launch_f32_to(const float* src, void* out, int out_dtype, Lay out_l,
+                          int B, int N, int H, int d, float mul, cudaStream_t st);
 // Padded rows of a [B, N, H, d] tensor (row l of host i with l >= host_len[i],
 // S = N / P rows per host) are set to zero, and lse[b, h, row] to -inf when
 // lse is given.
-cudaError_t launch_fill_padding(void* t, int dtype, long long bs, int B, int N, int H, int d,
+cudaError_t launch_fill_padding(void* t, int dtype, Lay l, int B, int N, int H, int d,
                                 int P, const int* host_len, float* lse, cudaStream_t st);
 cudaError_t launch_selftest_timeout(unsigned int timeout_us, int* status,
                                     cudaStream_t st);
@@ -140,9 +142,9 @@ struct TcFwdArgs {
   float* o_acc;     // block mode: [B, Nq, Hq, d] fp32
   float* m_acc;     // [B, Hq, Nq] (natural-log units)
   float* l_acc;
-  void* o_out;      // ring mode: [B, Nq, Hq, d] in o_dtype, batch stride o_bs
+  void* o_out;      // ring mode: [B, Nq, Hq, d] in o_dtype, layout ol
   int o_dtype;
-  long long o_bs;
+  Lay ol;
   float* lse;       // [B, Hq, Nq]
   int* status;
   unsigned long long wait_limit_ns;
@@ -170,10 +172,10 @@ struct TcBwdArgs {
   const float* lse;   // [B, Hq, N]: -LSE * log2(e)
   const float* Dvec;  // [B, Hq, N]: -D
   float* dq_acc;      // packed fp32 [B, N, Hq, d], pre-zeroed, reduce-added
-  void* dk;           // [B, N, Hkv, d] in grad_dtype, batch stride kv_bs
+  void* dk;           // [B, N, Hkv, d] in grad_dtype, layout kvl
   void* dv;
   int grad_dtype;
-  long long kv_bs;
+  Lay kvl;
   int* status;
   unsigned long long wait_limit_ns;
   int num_units;

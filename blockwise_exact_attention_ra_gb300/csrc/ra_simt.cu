@@ -94,14 +94,14 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32)
   const int b = (int)(row / ((long long)a.Nq * a.Hq));
   const int g = h / (a.Hq / a.Hkv);
 
-  const float* qr = a.q + b * a.q_bs + ((long long)i * a.Hq + h) * D;
+  const float* qr = a.q + lay_at(a.ql, b, i, h);
 #pragma unroll
   for (int t = 0; t < DPL; ++t) q_sh[w][lane + 32 * t] = qr[lane + 32 * t];
   __syncwarp();
 
-  const long long kv_row_stride = (long long)a.Hkv * D;
-  const float* kbase = a.k + b * a.kv_bs + (long long)g * D;
-  const float* vbase = a.v + b * a.kv_bs + (long long)g * D;
+  const long long kv_row_stride = a.kvl.rs;
+  const float* kbase = a.k + lay_at(a.kvl, b, 0, g);
+  const float* vbase = a.v + lay_at(a.kvl, b, 0, g);
 
   float m, l, o[DPL];
   const long long srow = ((long long)b * a.Hq + h) * a.Nq + i;       // m/l/lse index
@@ -131,7 +131,7 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32)
                           o);
     }
     const float inv = l > 0.f ? 1.f / l : 0.f;
-    const long long out_idx = b * a.o_bs + ((long long)i * a.Hq + h) * D;
+    const long long out_idx = lay_at(a.ql, b, i, h);
 #pragma unroll
     for (int t = 0; t < DPL; ++t) store_dtype(a.o_out, a.o_dtype, out_idx + lane + 32 * t, o[t] * inv);
     if (lane == 0) a.lse[srow] = l > 0.f ? m + logf(l) : -INFINITY;
@@ -169,7 +169,7 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32) simt_bwd_dq_kernel(const 
   const int h = (int)((row / a.N) % a.Hq);
   const int b = (int)(row / ((long long)a.N * a.Hq));
   const int g = h / (a.Hq / a.Hkv);
-  const long long qoff = b * a.q_bs + ((long long)i * a.Hq + h) * D;
+  const long long qoff = lay_at(a.ql, b, i, h);
 #pragma unroll
   for (int t = 0; t < DPL; ++t) {
     q_sh[w][lane + 32 * t] = a.q[qoff + lane + 32 * t];
@@ -179,9 +179,9 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32) simt_bwd_dq_kernel(const 
   const long long srow = ((long long)b * a.Hq + h) * a.N + i;
   const float lse = a.lse[srow];
   const float Di = a.Dvec[srow];
-  const long long rs = (long long)a.Hkv * D;
-  const float* kbase = a.k + b * a.kv_bs + (long long)g * D;
-  const float* vbase = a.v + b * a.kv_bs + (long long)g * D;
+  const long long rs = a.kvl.rs;
+  const float* kbase = a.k + lay_at(a.kvl, b, 0, g);
+  const float* vbase = a.v + lay_at(a.kvl, b, 0, g);
   float dq[DPL];
 #pragma unroll
   for (int t = 0; t < DPL; ++t) dq[t] = 0.f;
@@ -240,7 +240,7 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32) simt_bwd_dkdv_kernel(cons
   const int j = (int)(row % a.N);
   const int g = (int)((row / a.N) % a.Hkv);
   const int b = (int)(row / ((long long)a.N * a.Hkv));
-  const long long koff = b * a.kv_bs + ((long long)j * a.Hkv + g) * D;
+  const long long koff = lay_at(a.kvl, b, j, g);
 #pragma unroll
   for (int t = 0; t < DPL; ++t) {
     k_sh[w][lane + 32 * t] = a.k[koff + lane + 32 * t];
@@ -248,7 +248,7 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32) simt_bwd_dkdv_kernel(cons
   }
   __syncwarp();
   const int group = a.Hq / a.Hkv;
-  const long long qrs = (long long)a.Hq * D;
+  const long long qrs = a.ql.rs;
   float dk[DPL], dv[DPL];
 #pragma unroll
   for (int t = 0; t < DPL; ++t) dk[t] = dv[t] = 0.f;
@@ -256,8 +256,8 @@ __global__ void __launch_bounds__(kWarpsPerBlock * 32) simt_bwd_dkdv_kernel(cons
   const bool padded = a.host_len && (j - hj * a.S) >= clamp_len(a.host_len, hj, a.S);
   for (int hh = 0; hh < group && !padded; ++hh) {
     const int h = g * group + hh;
-    const float* qbase = a.q + b * a.q_bs + (long long)h * D;
-    const float* dobase = a.dO + b * a.q_bs + (long long)h * D;
+    const float* qbase = a.q + lay_at(a.ql, b, 0, h);
+    const float* dobase = a.dO + lay_at(a.ql, b, 0, h);
     const long long sbase = ((long long)b * a.Hq + h) * a.N;
     for (int s = 0; s < a.P; ++s) {
       const int host = (hj + s) % a.P;
@@ -356,7 +356,7 @@ __global__ void merge_kernel(float* oa, float* ma, float* la, const float* ob,
 }
 
 __global__ void finalize_kernel(const float* o, const float* m, const float* l, void* out,
-                                int out_dtype, long long out_bs, float* lse, int B, int N,
+                                int out_dtype, Lay out_l, float* lse, int B, int N,
                                 int H, int d) {
   const long long row = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
@@ -367,22 +367,34 @@ __global__ void finalize_kernel(const float* o, const float* m, const float* l, 
   const long long sidx = ((long long)b * H + h) * N + n;
   const float lv = l[sidx];
   const float inv = lv > 0.f ? 1.f / lv : 0.f;
-  const long long oidx = b * out_bs + ((long long)n * H + h) * d;
+  const long long oidx = lay_at(out_l, b, n, h);
   for (int c = lane; c < d; c += 32) store_dtype(out, out_dtype, oidx + c, o[row * d + c] * inv);
   if (lane == 0 && lse) lse[sidx] = lv > 0.f ? m[sidx] + logf(lv) : -INFINITY;
 }
 
-// 8 elements per thread; elems_per_batch % 8 == 0 and 16-byte aligned rows.
-template <typename T>
-__global__ void to_f16_kernel(const T* __restrict__ src, long long src_bs,
-                              __half* __restrict__ dst, int B, long long epb, int* status) {
-  const long long vecs = epb / 8;
-  const long long total = vecs * B;
+// 8 elements per thread; d % 8 == 0 and rows aligned to 8 elements.  The
+// destination is packed [B, N, H, d] (thread t writes elements 8t .. 8t+7).
+// Packed sources (rows of H*d elements) take the flat index within a batch;
+// other layouts decode (b, n, h) per vector.
+template <typename T, bool PACKED>
+__global__ void to_f16_kernel(const T* __restrict__ src, Lay src_l,
+                              __half* __restrict__ dst, int B, int N, int H, int d, int* status) {
+  const int vpr = d / 8;  // 8-element vectors per row
+  const long long vpb = (long long)N * H * vpr;  // per batch
+  const long long total = vpb * B;
   const long long stride = (long long)gridDim.x * blockDim.x;
   bool bad = false;
   for (long long t = (long long)blockIdx.x * blockDim.x + threadIdx.x; t < total; t += stride) {
-    const long long b = t / vecs, e = (t % vecs) * 8;
-    const T* s = src + b * src_bs + e;
+    const T* s;
+    if (PACKED) {
+      const long long b = t / vpb;
+      s = src + b * src_l.bs + (t - b * vpb) * 8;
+    } else {
+      const long long row = t / vpr;  // packed (b, n, h) row
+      const int h = (int)(row % H);
+      const long long bn = row / H;
+      s = src + lay_at(src_l, bn / N, bn % N, h) + (t - row * vpr) * 8;
+    }
     __align__(16) __half outv[8];
     if constexpr (sizeof(T) == 2) {
       const uint4 raw = *reinterpret_cast<const uint4*>(s);
@@ -401,13 +413,13 @@ __global__ void to_f16_kernel(const T* __restrict__ src, long long src_bs,
         outv[u] = __float2half_rn(f);
       }
     }
-    *reinterpret_cast<uint4*>(dst + b * epb + e) = *reinterpret_cast<const uint4*>(outv);
+    *reinterpret_cast<uint4*>(dst + t * 8) = *reinterpret_cast<const uint4*>(outv);
   }
   if (bad) report(status, RA_ERR_RANGE);
 }
 
 __global__ void bwd_dot_kernel(const void* dO, int do_dtype, const void* o, int o_dtype,
-                               long long q_bs, float* D, const float* lse, float* lse2, int B,
+                               Lay ql, float* D, const float* lse, float* lse2, int B,
                                int N, int H, int d) {
   const long long row = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
@@ -415,7 +427,7 @@ __global__ void bwd_dot_kernel(const void* dO, int do_dtype, const void* o, int 
   const int h = (int)(row % H);
   const int n = (int)((row / H) % N);
   const int b = (int)(row / ((long long)H * N));
-  const long long base = b * q_bs + ((long long)n * H + h) * d;
+  const long long base = lay_at(ql, b, n, h);
   float acc = 0.f;
   for (int c = lane; c < d; c += 32)
     acc = fmaf(load_dtype(dO, do_dtype, base + c), load_dtype(o, o_dtype, base + c), acc);
@@ -431,18 +443,31 @@ __global__ void bwd_dot_kernel(const void* dO, int do_dtype, const void* o, int 
   }
 }
 
+// Packed destinations: one element per thread, flat index within a batch.
 __global__ void f32_to_kernel(const float* __restrict__ src, void* out, int out_dtype,
                               long long out_bs, int B, long long epb, float mul) {
   const long long total = epb * B;
   const long long stride = (long long)gridDim.x * blockDim.x;
   for (long long t = (long long)blockIdx.x * blockDim.x + threadIdx.x; t < total; t += stride) {
-    const long long b = t / epb, e = t % epb;
+    const long long b = t / epb, e = t - b * epb;
     store_dtype(out, out_dtype, b * out_bs + e, src[t] * mul);
   }
 }
 
+// Other layouts: one warp per (b, n, h) row.
+__global__ void f32_to_rows_kernel(const float* __restrict__ src, void* out, int out_dtype,
+                                   Lay out_l, int B, int N, int H, int d, float mul) {
+  const long long row = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (row >= (long long)B * N * H) return;
+  const int h = (int)(row % H);
+  const long long bn = row / H;
+  const long long o = lay_at(out_l, bn / N, bn % N, h);
+  for (int c = lane; c < d; c += 32) store_dtype(out, out_dtype, o + c, src[row * d + c] * mul);
+}
+
 // One warp per (b, row): zero padded rows, set their LSE to -inf.
-__global__ void fill_padding_kernel(void* t, int dtype, long long bs, int B, int N, int H, int d,
+__global__ void fill_padding_kernel(void* t, int dtype, Lay l, int B, int N, int H, int d,
                                     int P, const int* host_len, float* lse) {
   const long long row = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
@@ -451,8 +476,10 @@ __global__ void fill_padding_kernel(void* t, int dtype, long long bs, int B, int
   const int S = N / P;
   const int host = n / S;
   if (n - host * S < clamp_len(host_len, host, S)) return;
-  const long long base = b * bs + (long long)n * H * d;
-  for (int c = lane; c < H * d; c += 32) store_dtype(t, dtype, base + c, 0.f);
+  for (int h = 0; h < H; ++h) {
+    const long long base = lay_at(l, b, n, h);
+    for (int c = lane; c < d; c += 32) store_dtype(t, dtype, base + c, 0.f);
+  }
   if (lse)
     for (int h = lane; h < H; h += 32) lse[((long long)b * H + h) * N + n] = -INFINITY;
 }
@@ -538,53 +565,63 @@ cudaError_t launch_merge(float* oa, float* ma, float* la, const float* ob, const
 }
 
 cudaError_t launch_finalize(const float* o, const float* m, const float* l, void* out,
-                            int out_dtype, long long out_bs, float* lse, int B, int N, int H,
+                            int out_dtype, Lay out_l, float* lse, int B, int N, int H,
                             int d, cudaStream_t st) {
   const long long rows = (long long)B * N * H;
-  finalize_kernel<<<grid_for(rows, 8), 256, 0, st>>>(o, m, l, out, out_dtype, out_bs, lse, B,
+  finalize_kernel<<<grid_for(rows, 8), 256, 0, st>>>(o, m, l, out, out_dtype, out_l, lse, B,
                                                       N, H, d);
   count_launch();
   return cudaGetLastError();
 }
 
-cudaError_t launch_to_f16(const void* src, int src_dtype, long long src_bs, void* dst, int B,
-                          long long epb, int* status, cudaStream_t st) {
-  const unsigned grid = grid_for(epb / 8 * B, 256 * 4);
-  if (src_dtype == RA_BF16)
-    to_f16_kernel<__nv_bfloat16><<<grid, 256, 0, st>>>(
-        static_cast<const __nv_bfloat16*>(src), src_bs, static_cast<__half*>(dst), B, epb,
-        status);
-  else if (src_dtype == RA_F32)
-    to_f16_kernel<float><<<grid, 256, 0, st>>>(static_cast<const float*>(src), src_bs,
-                                               static_cast<__half*>(dst), B, epb, status);
+template <typename T>
+void to_f16_launch(const T* src, Lay src_l, __half* dst, int B, int N, int H, int d, int* status,
+                   cudaStream_t st) {
+  const unsigned grid = grid_for((long long)B * N * H * (d / 8), 256 * 4);
+  if (src_l.rs == (long long)H * d && src_l.hs == d)
+    to_f16_kernel<T, true><<<grid, 256, 0, st>>>(src, src_l, dst, B, N, H, d, status);
   else
-    to_f16_kernel<__half><<<grid, 256, 0, st>>>(static_cast<const __half*>(src), src_bs,
-                                                static_cast<__half*>(dst), B, epb, status);
+    to_f16_kernel<T, false><<<grid, 256, 0, st>>>(src, src_l, dst, B, N, H, d, status);
+}
+
+cudaError_t launch_to_f16(const void* src, int src_dtype, Lay src_l, void* dst, int B, int N,
+                          int H, int d, int* status, cudaStream_t st) {
+  if (src_dtype == RA_BF16)
+    to_f16_launch(static_cast<const __nv_bfloat16*>(src), src_l, static_cast<__half*>(dst), B, N, H, d,
+                  status, st);
+  else if (src_dtype == RA_F32)
+    to_f16_launch(static_cast<const float*>(src), src_l, static_cast<__half*>(dst), B, N, H, d, status, st);
+  else
+    to_f16_launch(static_cast<const __half*>(src), src_l, static_cast<__half*>(dst), B, N, H, d, status, st);
   count_launch();
   return cudaGetLastError();
 }
 
 cudaError_t launch_bwd_dot(const void* dO, int do_dtype, const void* o, int o_dtype,
-                           long long q_bs, float* D, const float* lse, float* lse2, int B,
+                           Lay ql, float* D, const float* lse, float* lse2, int B,
                            int N, int H, int d, cudaStream_t st) {
   const long long rows = (long long)B * N * H;
-  bwd_dot_kernel<<<grid_for(rows, 8), 256, 0, st>>>(dO, do_dtype, o, o_dtype, q_bs, D, lse,
+  bwd_dot_kernel<<<grid_for(rows, 8), 256, 0, st>>>(dO, do_dtype, o, o_dtype, ql, D, lse,
                                                      lse2, B, N, H, d);
   count_launch();
   return cudaGetLastError();
 }
 
-cudaError_t launch_f32_to(const float* src, void* out, int out_dtype, long long out_bs, int B,
-                          long long epb, float mul, cudaStream_t st) {
-  f32_to_kernel<<<grid_for(epb * B, 256 * 8), 256, 0, st>>>(src, out, out_dtype, out_bs, B,
-                                                             epb, mul);
+cudaError_t launch_f32_to(const float* src, void* out, int out_dtype, Lay out_l, int B, int N,
+                          int H, int d, float mul, cudaStream_t st) {
+  const long long epb = (long long)N * H * d;
+  if (out_l.rs == (long long)H * d && out_l.hs == d)
+    f32_to_kernel<<<grid_for(epb * B, 256 * 8), 256, 0, st>>>(src, out, out_dtype, out_l.bs, B, epb, mul);
+  else
+    f32_to_rows_kernel<<<grid_for((long long)B * N * H, 8), 256, 0, st>>>(src, out, out_dtype, out_l, B, N,
+                                                                           H, d, mul);
   count_launch();
   return cudaGetLastError();
 }
 
-cudaError_t launch_fill_padding(void* t, int dtype, long long bs, int B, int N, int H, int d, int P,
+cudaError_t launch_fill_padding(void* t, int dtype, Lay l, int B, int N, int H, int d, int P,
                                 const int* host_len, float* lse, cudaStream_t st) {
-  fill_padding_kernel<<<grid_for((long long)B * N, 8), 256, 0, st>>>(t, dtype, bs, B, N, H, d, P, host_len,
+  fill_padding_kernel<<<grid_for((long long)B * N, 8), 256, 0, st>>>(t, dtype, l, B, N, H, d, P, host_len,
                                                                       lse);
   count_launch();
   return cudaGetLastError();

@@ -12,13 +12,14 @@
  *
  * Conventions shared by every entry point
  * ---------------------------------------
- * Layout.  q, k, v, o, dO, dq, dk, dv are [B, N, H, d] with d contiguous and
- *   heads at stride d (the pages' [seq, heads, head_dim] layout with a batch
- *   axis; "Building Ring Attention in PyTorch: The 200-Line Version").  The
- *   batch stride is ra_shape.q_bstride / kv_bstride (elements; 0 means
- *   packed).  Row blocks of a larger tensor are therefore plain pointer
- *   offsets.  The fp32 running state is o_acc [B, N_q, Hq, d] (packed) and
- *   m_acc, l_acc, lse [B, Hq, N_q] (packed).
+ * Layout.  q, k, v, o, dO, dq, dk, dv are [B, N, H, d] with d contiguous; by
+ *   default packed with heads at stride d (the pages' [seq, heads, head_dim]
+ *   layout with a batch axis; "Building Ring Attention in PyTorch: The
+ *   200-Line Version"), and any batch, row and head strides through ra_shape
+ *   (see there), so [B, H, N, d] tensors and slices of a fused projection
+ *   need no copy.  Row blocks of a larger tensor are plain pointer offsets.
+ *   The fp32 running state is o_acc [B, N_q, Hq, d] (packed) and m_acc,
+ *   l_acc, lse [B, Hq, N_q] (packed).
  * Scores.  s_ij = scale * q_i . k_j; scale is usually d^-0.5 (same section).
  *   With RA_CAUSAL in `flags` key j is visible to query i iff
  *   kv_pos(j) <= q_pos(i), positions being global row indices (q_off /
@@ -100,6 +101,21 @@ typedef enum {
   RA_ERR_TIMEOUT = 5      /* device: a bounded wait gave up */
 } ra_status;
 
+/* Sizes and strides.  The q group (q, o, dO, dq) and the kv group (k, v, dk,
+ * dv) each share one layout: element (b, n, h, c) of a q-group tensor sits at
+ * b * q_bstride + n * q_rstride + h * q_hstride + c (elements; d is always
+ * contiguous), and likewise for the kv group.  A stride of 0 takes its packed
+ * default: row stride H*d, head stride d, batch stride the extent of one
+ * batch ((N-1)*rstride + (H-1)*hstride + d).  So zeroed strides describe the
+ * pages' [seq, heads, head_dim] rows with a batch axis, and
+ *   [B, H, N, d] tensors:  rstride = d, hstride = N*d, bstride = H*N*d;
+ *   a slice of a fused [B, N, 3, H, d] projection: rstride = 3*H*d,
+ *   hstride = d, bstride = N*3*H*d (outputs of the group need the same
+ *   strides).
+ * Strides must not make two (n, h) rows overlap, nor one batch overlap the
+ * next; for 16-bit inputs on the tensor cores every stride is a multiple of 8
+ * elements (16 bytes).  The fp32 running state o_acc/m_acc/l_acc and lse are
+ * always packed.  Violations return RA_ERR_INVALID_ARG. */
 typedef struct {
   int B;                /* batch */
   int N_q;              /* query rows covered by the call */
@@ -107,8 +123,12 @@ typedef struct {
   int Hq;               /* query heads */
   int Hkv;              /* key/value heads (divides Hq) */
   int d;                /* head dimension */
-  long long q_bstride;  /* elements between batches of q/o/dO/dq; 0 = N_q*Hq*d */
-  long long kv_bstride; /* elements between batches of k/v/dk/dv; 0 = N_kv*Hkv*d */
+  long long q_bstride;  /* elements between batches of q/o/dO/dq; 0 = packed */
+  long long kv_bstride; /* elements between batches of k/v/dk/dv; 0 = packed */
+  long long q_rstride;  /* elements between rows (positions) of q/o/dO/dq; 0 = Hq*d */
+  long long q_hstride;  /* elements between heads of q/o/dO/dq; 0 = d */
+  long long kv_rstride; /* elements between rows of k/v/dk/dv; 0 = Hkv*d */
+  long long kv_hstride; /* elements between heads of k/v/dk/dv; 0 = d */
 } ra_shape;
 
 /* Set the running state to "nothing seen": o_acc = 0, m_acc = -inf,

@@ -167,3 +167,41 @@ def test_visit_log_arguments_are_checked(ra):
     assert lib.ra_debug_visit_log(ctypes.c_void_p(4104), 16, ctypes.c_void_p(8192)) == 1
     assert "aligned" in ra.ra_last_error()
     assert lib.ra_debug_visit_log(None, 0, None) == 0
+
+
+def test_strides_are_checked_without_a_gpu(ra):
+    lib = ra.lib
+    vp = ctypes.c_void_p(16)
+    assert len(ra.RaShape._fields_) == 12   # the header's ra_shape
+    bad = (
+        ra.RaShape(1, 256, 256, 2, 2, 64, 0, 0, 64, 64, 0, 0),      # rows and heads at the same stride
+        ra.RaShape(1, 256, 256, 2, 2, 64, 0, 0, 32, 0, 0, 0),       # row stride shorter than a row
+        ra.RaShape(1, 256, 256, 2, 2, 64, 0, 0, 64, 100, 0, 0),     # heads overlap the row block
+        ra.RaShape(1, 256, 256, 2, 2, 64, 0, 0, -64, 0, 0, 0),      # negative stride
+        ra.RaShape(2, 256, 256, 2, 2, 64, 1000, 0, 0, 0, 0, 0),     # batch shorter than its extent
+        ra.RaShape(1, 256, 256, 2, 2, 64, 0, 0, 0, 0, 0, 32),       # kv heads overlap
+    )
+    for sh in bad:
+        rc = lib.ra_ring_fwd(vp, vp, vp, ra.RA_BF16, sh, 1, 1, 0.1, vp, ra.RA_F32, vp, None, 0, None)
+        assert rc == 1, (sh.q_rstride, sh.q_hstride, sh.kv_hstride)
+        assert "stride" in ra.ra_last_error()
+    # the host-buffer step takes packed rows only; [B, H, N, d] host tensors are refused
+    hm = ra.RaShape(1, 256, 256, 2, 2, 64, 0, 0, 64, 256 * 64, 64, 256 * 64)
+    ws = ctypes.c_void_p(1 << 20)
+    rc = lib.ra_ring_step_host(vp, vp, vp, vp, ra.RA_BF16, hm, 2, 1, 0.1, vp, ra.RA_F32, vp, vp, vp, vp,
+                               ra.RA_F32, ws, 1 << 40, None)
+    assert rc == 2 and "packed rows" in ra.ra_last_error()
+
+
+def test_binding_passes_tensor_strides(ra):
+    import torch
+    x = torch.zeros(2, 4, 96, 64)                         # [B, H, N, d]
+    q = x.permute(0, 2, 1, 3)                             # viewed as [B, N, H, d]
+    sh = ra.shape_of(q, q)
+    assert (sh.q_bstride, sh.q_rstride, sh.q_hstride) == (4 * 96 * 64, 64, 96 * 64)
+    one = torch.zeros(1, 96, 1, 64)
+    sh1 = ra.shape_of(one, one)
+    assert (sh1.q_bstride, sh1.q_hstride) == (0, 0)      # extent-1 axes take the default
+    with pytest.raises(ra.RAError):
+        ra._same_layout(torch.zeros(2, 96, 4, 64), q, "o", "q")
+    assert ra.empty_like_layout(q).stride() == q.stride()
