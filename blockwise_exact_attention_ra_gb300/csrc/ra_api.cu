@@ -628,10 +628,11 @@ static int ring_fwd_impl(const void* q, const void* k, const void* v, ra_dtype d
   return e == cudaSuccess ? RA_OK : cuda_fail(e, "tensor-core ring forward launch");
 }
 
-// Backward workspace: D [B,Hq,N] fp32 | dq_acc [B,N,Hq,d] fp32 |
+// Backward workspace: D [B,Hq,N] fp32 | LSE*log2e [B,Hq,N] fp32 |
+// dq_acc [B,N,Hq,d] fp32 | unit counter (256 bytes, zeroed with dq_acc) |
 // fp16 copies of q, k, v, dO (16-bit dtypes that are not already fp16).
 struct BwdWs {
-  size_t D, lse2, dq, q16, k16, v16, do16, total;
+  size_t D, lse2, dq, sched, q16, k16, v16, do16, total;
 };
 static BwdWs bwd_layout(int dtype, const ra_shape& sh) {
   BwdWs w{};
@@ -642,6 +643,7 @@ static BwdWs bwd_layout(int dtype, const ra_shape& sh) {
   if (dtype != RA_F32) {
     w.lse2 = off; off += align256((size_t)sh.B * sh.Hq * sh.N_q * 4);
     w.dq = off; off += align256(qel * 4);
+    w.sched = off; off += 256;
     if (dtype == RA_BF16) {
       w.q16 = off; off += align256(qel * 2);
       w.k16 = off; off += align256(kvel * 2);
@@ -715,7 +717,6 @@ static int ring_bwd_impl(const void* q, const void* k, const void* v, const void
     return e == cudaSuccess ? RA_OK : cuda_fail(e, "fp32 ring backward launch");
   }
   if ((rc = check_tc(s, dtype))) return rc;
-  const long long qel = (long long)s.Nq * s.Hq * s.d, kvel = (long long)s.Nkv * s.Hkv * s.d;
   float* lse2 = reinterpret_cast<float*>(ws + w.lse2);
   cudaError_t e = launch_bwd_dot(dO, dtype, o, o_dtype, s.ql, Dv, lse, lse2, s.B, s.Nq, s.Hq,
                                  s.d, cs);
@@ -733,7 +734,7 @@ static int ring_bwd_impl(const void* q, const void* k, const void* v, const void
       return cuda_fail(e, "fp16 operand copy launch");
   }
   float* dq_acc = reinterpret_cast<float*>(ws + w.dq);
-  e = cudaMemsetAsync(dq_acc, 0, (size_t)s.B * qel * 4, cs);
+  e = cudaMemsetAsync(dq_acc, 0, w.sched + 256 - w.dq, cs);  // and the unit counter
   if (e != cudaSuccess) return cuda_fail(e, "zero dq accumulator");
   TcBwdArgs a;
   memset(&a, 0, sizeof a);
@@ -762,6 +763,7 @@ static int ring_bwd_impl(const void* q, const void* k, const void* v, const void
   a.wait_limit_ns = wait_limit_ns();
   a.log = visit_log();
   a.num_units = s.B * s.Hkv * (s.Nkv / 128);
+  a.sched = reinterpret_cast<unsigned int*>(ws + w.sched);
   {
     TimedLaunch tl(RA_KERNEL_BWD_TC, cs);
     e = launch_tc_bwd(a, device_sms(), cs);

@@ -72,10 +72,11 @@ struct BwdSmem {
   static constexpr int kBars = kVec0 + 2 * 1024;
   // kv_full, kv_empty, q_full[2], q_empty[2], s_full, dp_full, ds_full,
   // ds_free, dq_full, dq_free, dkv_full, dkv_free, drain, (unused),
-  // do_full[2], do_empty[2], (unused), p_full
-  static constexpr int kNumBars = 22;
-  static constexpr int kMisc = kBars + kNumBars * 8;
-  static constexpr int kUsed = kMisc + 16;
+  // do_full[2], do_empty[2], (unused), p_full, unit_full[4], unit_empty[4]
+  static constexpr int kNumBars = 30;
+  static constexpr int kMisc = kBars + kNumBars * 8;  // TMEM address, abort flag
+  static constexpr int kUnits = kMisc + 16;           // unit ring: 4 unit indices
+  static constexpr int kUsed = kUnits + 16;
   // at least 120 KB so that one CTA (holding all 512 TMEM columns) occupies an SM
   static constexpr int kBytes = kUsed > 122880 ? kUsed : 122880;
 };
@@ -92,22 +93,14 @@ struct BwdUnit {
 // (batch, key/value head) at a time, so the query tiles, dO tiles and dQ
 // accumulator rows they sweep stay in L2 (one head of them is ~128 MB at
 // N = 131072).  Within a head the earliest key tiles come first: under a
-// causal mask they have the most work.
+// causal mask they have the most work.  The CTAs draw units in this order
+// from a counter in global memory, so a CTA that finishes early takes the
+// next unit instead of running ahead into another head, and the lightest
+// units end the launch.
 __device__ __forceinline__ int host_len_at(const int* hl, int j, int S);
 
 template <bool STRIPED, bool VARLEN>
 __device__ __forceinline__ BwdUnit bwd_unit(const TcBwdArgs& a, int u) {
-  // CTA b takes units b, b + G, b + 2G, ... (G CTAs).  Odd rounds run in
-  // reverse, so the CTA that drew the heaviest unit of one round draws the
-  // lightest of the next: every CTA gets the same work per pair of rounds and
-  // they sweep the same head together, keeping its Q, dO and dQ lines in L2.
-  {
-    const int G = gridDim.x, rnd = u / G;
-    if (rnd & 1) {
-      const int in_round = min(G, a.num_units - rnd * G);
-      u = rnd * G + (in_round - 1 - (u - rnd * G));
-    }
-  }
   BwdUnit r;
   const int nT = a.N / 128;
   const int bg = u / nT;
@@ -239,6 +232,9 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
   auto bar_do_full = [&](int s) { return bar0 + 128 + 8 * s; };
   auto bar_do_empty = [&](int s) { return bar0 + 144 + 8 * s; };
   const uint32_t BAR_P_FULL = bar0 + 168;
+  auto bar_unit_full = [&](int s) { return bar0 + 176 + 8 * s; };
+  auto bar_unit_empty = [&](int s) { return bar0 + 208 + 8 * s; };
+  volatile int* unit_ring = reinterpret_cast<volatile int*>(smem + L::kUnits);
   const uint32_t BAR_S_FULL = bar0 + 48, BAR_DP_FULL = bar0 + 56, BAR_DS_FULL = bar0 + 64,
                  BAR_DS_FREE = bar0 + 72, BAR_DQ_FULL = bar0 + 80, BAR_DQ_FREE = bar0 + 88,
                  BAR_DKV_FULL = bar0 + 96, BAR_DKV_FREE = bar0 + 104, BAR_DRAIN = bar0 + 112;
@@ -266,6 +262,13 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
     mbar_init(BAR_DKV_FREE, 128);
     mbar_init(BAR_DRAIN, 1);
     mbar_init(BAR_P_FULL, 256);
+    // the producer draws the CTA's units and passes them on through a ring of
+    // four slots; every consumer thread (MMA lane, 256 compute and 128 dQ
+    // threads) hands a slot back once it has read it
+    for (int s = 0; s < 4; ++s) {
+      mbar_init(bar_unit_full(s), 1);
+      mbar_init(bar_unit_empty(s), 1 + 256 + 128);
+    }
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -286,6 +289,15 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
   const uint32_t tmem = *tmem_slot;
   const uint64_t lim = a.wait_limit_ns;
   const uint32_t T_S = tmem, T_DP = tmem + 128, T_DK = tmem + 256, T_DV = tmem + 256 + D;
+  // The n-th unit of this CTA, as the producer drew it (every role but the
+  // producer); false if the wait gave up.
+  auto take_unit = [&](int n, int* u) {
+    const int slot = n & 3;
+    if (!mbar_wait(bar_unit_full(slot), (n >> 2) & 1, abort_flag, a.status, lim)) return false;
+    *u = unit_ring[slot];
+    mbar_arrive(bar_unit_empty(slot));
+    return true;
+  };
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -296,11 +308,18 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
       int q_issued[2] = {0, 0}, do_issued[2] = {0, 0};
       int k = 0;
       bool ok = true;
-      // k counts the units this CTA has worked on; a key tile wholly in
-      // padding is no unit
-      for (int u = blockIdx.x; u < a.num_units && ok; u += gridDim.x, ++k) {
+      // n counts the units this CTA has drawn, k those it has worked on (a
+      // key tile wholly in padding is no unit); a draw at or past the last
+      // unit ends every role
+      for (int n = 0; ok; ++n) {
+        const int slot = n & 3;
+        if (!mbar_wait(bar_unit_empty(slot), ((n >> 2) & 1) ^ 1, abort_flag, a.status, lim)) { ok = false; break; }
+        const int u = (int)atomicAdd(a.sched, 1u);
+        unit_ring[slot] = u;
+        mbar_arrive(bar_unit_full(slot));
+        if (u >= a.num_units) break;
         const BwdUnit bu = bwd_unit<STRIPED, VARLEN>(a, u);
-        if (VARLEN && bu.n_iter == 0) { --k; continue; }
+        if (VARLEN && bu.n_iter == 0) continue;
         if (!mbar_wait(BAR_KV_EMPTY, (k & 1) ^ 1, abort_flag, a.status, lim)) { ok = false; break; }
         mbar_arrive_expect_tx(BAR_KV_FULL, 2 * L::kTile);
 #pragma unroll
@@ -308,6 +327,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
           tma_load_4d(sbase + L::kK + c * 16384, &a.tm_k, BAR_KV_FULL, c * 64, bu.g, bu.jt * 128, bu.b, pol_kv);
           tma_load_4d(sbase + L::kV + c * 16384, &a.tm_v, BAR_KV_FULL, c * 64, bu.g, bu.jt * 128, bu.b, pol_kv);
         }
+        ++k;
         for (int it = 0; it < bu.n_iter; ++it) {
           int h, qt;
           bwd_iter<STRIPED>(a, bu, it, &h, &qt);
@@ -386,9 +406,11 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
         }
         return it;
       };
-      for (int u = blockIdx.x; u < a.num_units && ok; u += gridDim.x, ++k) {
+      for (int n = 0; ok; ++n) {
+        int u;
+        if (!take_unit(n, &u) || u >= a.num_units) break;
         const BwdUnit bu = bwd_unit<STRIPED, VARLEN>(a, u);
-        if (VARLEN && bu.n_iter == 0) { --k; continue; }
+        if (VARLEN && bu.n_iter == 0) continue;
         if (!wait(BAR_KV_FULL, k & 1)) break;
         // prologue: S(0), dP(0)
         uint32_t s = qd_cnt & 1;
@@ -498,6 +520,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
             mma_commit(BAR_KV_EMPTY);
           }
         }
+        ++k;
       }
       mma_commit(BAR_DRAIN);
       (void)mbar_wait(BAR_DRAIN, 0, abort_flag, nullptr, 100000000ull);
@@ -514,7 +537,9 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
     uint8_t* ds_row = smem + L::kDS + half * 16384 + r * 128;
     uint32_t gi = 0;  // iterations done by this CTA (all units)
     bool ok = true;
-    for (int u = blockIdx.x; u < a.num_units && ok; u += gridDim.x) {
+    for (int n = 0; ok; ++n) {
+      int u;
+      if (!take_unit(n, &u) || u >= a.num_units) break;
       const BwdUnit bu = bwd_unit<STRIPED, VARLEN>(a, u);
       // padding: key rows of this tile from kvalid on (variable host lengths)
       int kvalid = 128;
@@ -523,9 +548,14 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
         const int j = div_by(bu.jt, a.T_m);
         kvalid = host_len_at(a.host_len, j, a.ring_S) - (bu.jt - j * T) * 128;
       }
+      // kq: position in the current query head's sweep, enough to place the
+      // diagonal tiles without the query tile index
+      int kq = 0;
       for (int it = 0; it < bu.n_iter; ++it, ++gi) {
-        int h, qt;
-        bwd_iter<STRIPED>(a, bu, it, &h, &qt);
+        const int kpos = kq;
+        if (++kq == bu.count) kq = 0;
+        int h = 0, qt = 0;
+        if (VARLEN) bwd_iter<STRIPED>(a, bu, it, &h, &qt);
         // padding: query columns of this tile from qvalid on; a tile wholly in
         // padding is skipped by every role
         int qvalid = 128;
@@ -548,19 +578,18 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
         RA_TMEM_LD32(tS + 32, (pr + 32));
         tmem_ld_wait();
         // causal masks: the diagonal tile of a contiguous layout (query column
-        // c visible to key row r iff c >= r); for a striped layout the same
-        // local tile of any host pair, strict (c > r) when the key's host
-        // comes after the query's
+        // c visible to key row r iff c >= r), the first of the sweep; for a
+        // striped layout the same local tile of any host pair, the sweep's
+        // first lap (query hosts j, j+1, ... in ring order), strict (c > r)
+        // where the query's host index has wrapped below the key's
         const bool pad = VARLEN && (qvalid < 128 || kvalid < 128);
         bool diag;
         int strict = 0;
         if (STRIPED) {
-          const int T_local = a.ring_S / 128;
-          const int qhost = div_by(qt, a.T_m);
-          diag = qt - qhost * T_local == bu.tk;
-          strict = bu.host > qhost ? 1 : 0;
+          diag = kpos < a.ring_P;
+          strict = bu.host + kpos >= a.ring_P ? 1 : 0;
         } else {
-          diag = a.causal && qt == bu.jt;
+          diag = a.causal && kpos == 0;
         }
         // P^T = exp2(S^T * scale*log2e - LSE*log2e), two columns per fp32x2 FMA
         const float2 sl2x2 = make_float2(sl2, sl2);
@@ -649,9 +678,11 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
     uint32_t dq_cnt = 0;
     int k = 0;
     bool ok = true;
-    for (int u = blockIdx.x; u < a.num_units && ok; u += gridDim.x, ++k) {
+    for (int n = 0; ok; ++n) {
+      int u;
+      if (!take_unit(n, &u) || u >= a.num_units) break;
       const BwdUnit bu = bwd_unit<STRIPED, VARLEN>(a, u);
-      if (VARLEN && bu.n_iter == 0) { --k; continue; }
+      if (VARLEN && bu.n_iter == 0) continue;
       for (int it = 0; it < bu.n_iter; ++it) {
         int h, qt;
         bwd_iter<STRIPED>(a, bu, it, &h, &qt);
@@ -754,6 +785,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_bwd_kernel(const __grid_consta
       }
       tc_fence_before();
       mbar_arrive(BAR_DKV_FREE);
+      ++k;
     }
     if (lane == 0) bulk_wait_all();  // this warp's reductions complete before the CTA exits
   }

@@ -179,6 +179,7 @@ struct TcBwdArgs {
   int* status;
   unsigned long long wait_limit_ns;
   int num_units;
+  unsigned int* sched;  // unit counter the CTAs draw from; zero at launch
   VisitLog log;     // debug record of the query tiles loaded (off when log.entries is NULL)
 };
 cudaError_t launch_tc_bwd(TcBwdArgs& a, int num_sms, cudaStream_t st);
