@@ -536,10 +536,14 @@ int ra_block_fwd(const void* q, const void* k_blk, const void* v_blk, ra_dtype d
   return e == cudaSuccess ? RA_OK : cuda_fail(e, "tensor-core block forward launch");
 }
 
+// Ring forward workspace (16-bit dtypes): unit counter (256 bytes) | fp16
+// copy of V [B,N,Hkv,d] (bf16 inputs).
 size_t ra_ring_fwd_workspace_bytes(ra_dtype dtype, ra_shape shape, int P) {
   (void)P;
-  if (dtype != RA_BF16 || shape.B < 1 || shape.N_kv < 1 || shape.Hkv < 1 || shape.d < 1) return 0;
-  return align256((size_t)shape.B * shape.N_kv * shape.Hkv * shape.d * 2);
+  if ((dtype != RA_BF16 && dtype != RA_F16) || shape.B < 1 || shape.N_kv < 1 || shape.Hkv < 1 || shape.d < 1)
+    return 0;
+  if (dtype == RA_F16) return 256;
+  return 256 + align256((size_t)shape.B * shape.N_kv * shape.Hkv * shape.d * 2);
 }
 
 static int check_ring(const Shape& s, int P, int dtype) {
@@ -589,15 +593,19 @@ static int ring_fwd_impl(const void* q, const void* k, const void* v, ra_dtype d
     return e == cudaSuccess ? RA_OK : cuda_fail(e, "fp32 ring forward launch");
   }
   if ((rc = check_tc(s, dtype))) return rc;
+  const size_t need = ra_ring_fwd_workspace_bytes(dtype, shape, P);
+  if (!workspace || ws_bytes < need)
+    return fail(RA_ERR_INVALID_ARG, "workspace of %zu bytes needed (got %zu)", need, ws_bytes);
+  if ((rc = check_ptr(workspace, "workspace"))) return rc;
+  unsigned int* sched = static_cast<unsigned int*>(workspace);
+  cudaError_t me = cudaMemsetAsync(sched, 0, 256, cs);
+  if (me != cudaSuccess) return cuda_fail(me, "zero unit counter");
   const void* v16 = v;
   if (dtype == RA_BF16) {
-    const size_t need = ra_ring_fwd_workspace_bytes(dtype, shape, P);
-    if (!workspace || ws_bytes < need)
-      return fail(RA_ERR_INVALID_ARG, "workspace of %zu bytes needed (got %zu)", need, ws_bytes);
-    if ((rc = check_ptr(workspace, "workspace"))) return rc;
-    cudaError_t e = launch_to_f16(v, RA_BF16, s.kvl, workspace, s.B, s.Nkv, s.Hkv, s.d, st, cs);
+    void* vcopy = static_cast<char*>(workspace) + 256;
+    cudaError_t e = launch_to_f16(v, RA_BF16, s.kvl, vcopy, s.B, s.Nkv, s.Hkv, s.d, st, cs);
     if (e != cudaSuccess) return cuda_fail(e, "v -> fp16 launch");
-    v16 = workspace;
+    v16 = vcopy;
   }
   TcFwdArgs a;
   memset(&a, 0, sizeof a);
@@ -623,6 +631,7 @@ static int ring_fwd_impl(const void* q, const void* k, const void* v, ra_dtype d
   a.log = visit_log();
   const int T = a.ring_S / 128;
   a.num_units = s.B * s.Hq * P * ((T + 1) / 2);
+  a.sched = sched;
   TimedLaunch tl(RA_KERNEL_FWD_TC, cs);
   cudaError_t e = launch_tc_fwd(a, device_sms(), cs);
   return e == cudaSuccess ? RA_OK : cuda_fail(e, "tensor-core ring forward launch");

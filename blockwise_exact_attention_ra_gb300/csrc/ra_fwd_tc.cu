@@ -58,10 +58,11 @@ struct FwdSmem {
   static constexpr int kStage0 = 2 * kTileBytes;
   static constexpr int kBars = kStage0 + kStages * kTileBytes;
   // barriers: q_full, q_empty, kv_full[S], kv_empty[S], s_full[2], p_full[2],
-  // o_full[2], drain
-  static constexpr int kNumBars = 2 + 2 * kStages + 6 + 1;
+  // o_full[2], drain, unit_full[4], unit_empty[4]
+  static constexpr int kNumBars = 2 + 2 * kStages + 6 + 1 + 8;
   static constexpr int kMisc = kBars + kNumBars * 8;  // tmem slot, abort flag
-  static constexpr int kBytes = kMisc + 16;
+  static constexpr int kUnits = kMisc + 16;           // unit ring: 4 unit indices
+  static constexpr int kBytes = kUnits + 16;
   // slack for 1024-byte alignment; at least 120 KB so that one CTA (holding
   // all 512 TMEM columns) occupies an SM
   static constexpr int kAlloc = (kBytes + 1024) > 122880 ? (kBytes + 1024) : 122880;
@@ -153,7 +154,9 @@ __device__ __forceinline__ int last_visible_tile(const TcFwdArgs& a, long long q
 // Units are ordered head-major (all resident CTAs sweep the key/value tiles
 // of one (batch, head) together, which keeps them in L2), and within a head
 // from the last query tiles to the first: under a causal mask the last ones
-// see the most keys.
+// see the most keys.  The ring forward's CTAs draw units in this order from
+// a counter in global memory, so none runs ahead into another head and the
+// lightest units end the launch.
 // VARLEN selects the kernel built for variable host lengths; the other
 // builds see no length array and compile its checks away.
 template <bool VARLEN>
@@ -281,6 +284,9 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
   auto bar_p_full = [&](int x) { return bar_x + 16 + 8 * x; };
   auto bar_o_full = [&](int x) { return bar_x + 32 + 8 * x; };
   const uint32_t BAR_DRAIN = bar_x + 48;
+  auto bar_unit_full = [&](int s) { return bar_x + 56 + 8 * s; };
+  auto bar_unit_empty = [&](int s) { return bar_x + 88 + 8 * s; };
+  volatile int* unit_ring = reinterpret_cast<volatile int*>(smem + L::kUnits);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::kMisc + 4);
 
@@ -300,6 +306,13 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
       mbar_init(bar_o_full(x), 1);
     }
     mbar_init(BAR_DRAIN, 1);
+    // the producer draws the CTA's units and passes them on through a ring of
+    // four slots; every consumer thread (MMA lane, 256 softmax threads) hands
+    // a slot back once it has read it
+    for (int s = 0; s < 4; ++s) {
+      mbar_init(bar_unit_full(s), 1);
+      mbar_init(bar_unit_empty(s), 1 + 256);
+    }
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -317,6 +330,15 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const uint64_t lim = a.wait_limit_ns;
+  // The n-th unit of this CTA, as the producer drew it (every role but the
+  // producer); false if the wait gave up.
+  auto take_unit = [&](int n, int* u) {
+    const int slot = n & 3;
+    if (!mbar_wait(bar_unit_full(slot), (n >> 2) & 1, abort_flag, a.status, lim)) return false;
+    *u = unit_ring[slot];
+    mbar_arrive(bar_unit_empty(slot));
+    return true;
+  };
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -330,7 +352,15 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
       int issued[kStages];
       for (int s = 0; s < kStages; ++s) issued[s] = 0, last_phase[s] = 0;
       int q_issued = 0;
-      for (int u = blockIdx.x; u < a.num_units && ok; u += gridDim.x) {
+      // n counts the units this CTA has drawn; a draw at or past the last
+      // unit ends every role
+      for (int n = 0; ok; ++n) {
+        const int slot = n & 3;
+        if (!mbar_wait(bar_unit_empty(slot), ((n >> 2) & 1) ^ 1, abort_flag, a.status, lim)) { ok = false; break; }
+        const int u = a.sched ? (int)atomicAdd(a.sched, 1u) : (int)blockIdx.x + n * (int)gridDim.x;
+        unit_ring[slot] = u;
+        mbar_arrive(bar_unit_full(slot));
+        if (u >= a.num_units) break;
         const UnitInfo ui = unit_info<VARLEN>(a, u);
         if (ui.n_iter == 0) continue;  // no key of this block is visible to the unit
         if (!mbar_wait(BAR_Q_EMPTY, (k & 1) ^ 1, abort_flag, a.status, lim)) { ok = false; break; }
@@ -412,7 +442,9 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
           for (int kk = 0; kk < 8; ++kk) mma_ts(tO[x], tS[x] + 64 + kk * 8, desc_off(db, kk * 2048), idesc_pv, 1u);
         }
       };
-      for (int u = blockIdx.x; u < a.num_units && ok; u += gridDim.x) {
+      for (int n = 0; ok; ++n) {
+        int u;
+        if (!take_unit(n, &u) || u >= a.num_units) break;
         const UnitInfo ui = unit_info<VARLEN>(a, u);
         if (ui.n_iter == 0) continue;
         if (!mbar_wait(BAR_Q_FULL, k & 1, abort_flag, a.status, lim)) { ok = false; break; }
@@ -474,7 +506,9 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
     const float sl2 = a.scale_log2;
     uint32_t s_cnt = 0, o_cnt = 0;
     bool ok = true;
-    for (int u = blockIdx.x; u < a.num_units && ok; u += gridDim.x) {
+    for (int n = 0; ok; ++n) {
+      int u;
+      if (!take_unit(n, &u) || u >= a.num_units) break;
       const UnitInfo ui = unit_info<VARLEN>(a, u);
       if ((VARLEN && ui.n_iter == 0) || !ever_active(ui, x)) continue;  // this tile sees no key in this unit
       const int row = ui.qa_row0 + x * 128 + r;  // tensor row

@@ -149,6 +149,7 @@ struct TcFwdArgs {
   int* status;
   unsigned long long wait_limit_ns;
   int num_units;    // work units (pairs of 128-row query tiles)
+  unsigned int* sched;  // unit counter the CTAs draw from, zero at launch; NULL: CTA c takes units c, c + grid, ...
   VisitLog log;     // debug record of the key/value tiles loaded (off when log.entries is NULL)
 };
 cudaError_t launch_tc_fwd(TcFwdArgs& a, int num_sms, cudaStream_t st);

@@ -1,7 +1,7 @@
 // ra_ring_fwd_noalloc: the ring forward for callers that cannot allocate
 // device memory (see include/ra.h).  The scratch that ra_ring_fwd takes as a
-// caller workspace (the fp16 copy of V for bf16 inputs) lives here in a
-// fixed, file-scope device array instead.
+// caller workspace (its unit counter and, for bf16 inputs, the fp16 copy of
+// V) lives here in a fixed, file-scope device array instead.
 #include <cuda_runtime.h>
 #include <stdio.h>
 
@@ -11,7 +11,8 @@
 
 namespace {
 
-constexpr size_t kScratchBytes = size_t(32) << 20;  // 32 MiB per device
+constexpr size_t kVBytes = size_t(32) << 20;         // room for the fp16 V copy
+constexpr size_t kScratchBytes = 256 + kVBytes;       // + the unit counter, per device
 
 // One copy per device that loads the library; it lives until the process
 // exits.  In host code `g_noalloc_scratch` names a host-side stand-in, not a
@@ -39,7 +40,7 @@ int ra_ring_fwd_noalloc(const void* q, const void* k, const void* v, ra_dtype dt
   // B * N_kv * Hkv * d * 2 bytes, compared without overflow: B < 2^31 and
   // N_kv * Hkv * d * 2 < 2^55
   const unsigned long long per_batch = (unsigned long long)shape.N_kv * shape.Hkv * shape.d * 2ull;
-  const bool too_big = dtype == RA_BF16 && (unsigned long long)shape.B > kScratchBytes / per_batch;
+  const bool too_big = dtype == RA_BF16 && (unsigned long long)shape.B > kVBytes / per_batch;
   const size_t need = too_big ? 0 : ra_ring_fwd_workspace_bytes(dtype, shape, P);
   if (too_big || need > kScratchBytes) {
     char msg[256];
@@ -47,7 +48,7 @@ int ra_ring_fwd_noalloc(const void* q, const void* k, const void* v, ra_dtype dt
       snprintf(msg, sizeof msg,
                "ra_ring_fwd_noalloc: this shape needs more scratch than the built-in buffer holds "
                "(%zu bytes); call ra_ring_fwd with a workspace instead",
-               kScratchBytes);
+               kScratchBytes);  // only bf16 shapes need more than the counter
     else
       snprintf(msg, sizeof msg,
                "ra_ring_fwd_noalloc: this shape needs %zu bytes of scratch but the built-in buffer "

@@ -180,6 +180,11 @@ int ra_finalize(const float* o_acc, const float* m_acc, const float* l_acc,
  * Version" with the rescaled merge).
  *   q [B, N, Hq, d], k, v [B, N, Hkv, d] with N = shape.N_q = shape.N_kv
  *   o [B, N, Hq, d] in o_dtype; lse [B, Hq, N] fp32 (natural log)
+ *   workspace: device memory, 256-byte aligned, at least
+ *   ra_ring_fwd_workspace_bytes() bytes: for bf16/fp16 a 256-byte counter
+ *   from which the kernel's CTAs draw their work (zeroed by each call), for
+ *   bf16 also the fp16 copy of V; fp32 needs none (NULL allowed).  It must
+ *   not be in use by work that overlaps the call on the GPU.
  * Tensor-core dtypes need S a multiple of 128. */
 int ra_ring_fwd(const void* q, const void* k, const void* v, ra_dtype dtype,
                 ra_shape shape, int P, int flags, float scale, void* o,
@@ -212,12 +217,13 @@ size_t ra_ring_bwd_workspace_bytes(ra_dtype dtype, ra_dtype grad_dtype,
  * device allocation, or with a fixed memory budget set at start-up) cannot
  * provide the workspace ra_ring_fwd asks for.  This entry point takes the
  * same arguments minus the workspace and uses a scratch buffer that is part
- * of the library itself: a 32 MiB device array per GPU that loads the
- * library, held until the process exits.  It allocates nothing.  The pages
+ * of the library itself: a device array of 32 MiB + 256 bytes per GPU that
+ * loads the library, held until the process exits.  It allocates nothing.  The pages
  * describe no counterpart; it is a packaging of the same computation.
- *   Limit: shapes whose ra_ring_fwd_workspace_bytes() exceeds 32 MiB (the
- *   fp16 copy of V for bf16 inputs, B*N*Hkv*d*2 bytes) are rejected with
- *   RA_ERR_INVALID_ARG; fp16 and fp32 inputs need no scratch.
+ *   Limit: shapes whose ra_ring_fwd_workspace_bytes() exceeds that size
+ *   (the 256-byte work counter plus, for bf16 inputs, the fp16 copy of V,
+ *   B*N*Hkv*d*2 bytes, at most 32 MiB) are rejected with RA_ERR_INVALID_ARG;
+ *   fp16 inputs use only the counter, fp32 inputs no scratch.
  *   When the memory is taken: the array sits in a device module of its own
  *   (no kernel shares it).  Under CUDA's lazy module loading (the default
  *   since CUDA 12.2) a device reserves the 32 MiB at this entry point's
@@ -229,8 +235,8 @@ size_t ra_ring_bwd_workspace_bytes(ra_dtype dtype, ra_dtype grad_dtype,
  *   (cudaGetSymbolAddress) with that device current; make that first call
  *   before any stream capture.
  *   All calls share the one buffer per device and it keeps whatever the last
- *   call left there (each call overwrites the part it uses, nothing needs to
- *   start at zero).  Calls whose work overlaps on the GPU (different streams,
+ *   call left there (each call zeroes the counter and overwrites the part it
+ *   uses).  Calls whose work overlaps on the GPU (different streams,
  *   or threads without ordering between them) race on it. */
 int ra_ring_fwd_noalloc(const void* q, const void* k, const void* v, ra_dtype dtype,
                         ra_shape shape, int P, int flags, float scale, void* o,

@@ -41,7 +41,7 @@ def test_library_exports_every_declared_symbol(ra):
 def test_workspace_sizes(ra):
     sh = ra.RaShape(1, 1024, 1024, 4, 2, 128, 0, 0)
     assert ra.ra_ring_fwd_workspace_bytes(ra.RA_BF16, sh, 4) >= 1024 * 2 * 128 * 2
-    assert ra.ra_ring_fwd_workspace_bytes(ra.RA_F16, sh, 4) == 0
+    assert ra.ra_ring_fwd_workspace_bytes(ra.RA_F16, sh, 4) == 256   # the unit counter
     assert ra.ra_ring_fwd_workspace_bytes(ra.RA_F32, sh, 4) == 0
     ws = ra.ra_ring_bwd_workspace_bytes(ra.RA_BF16, ra.RA_F32, sh, 4)
     # D, LSE*log2e, fp32 dq accumulator, fp16 copies of q, k, v, dO

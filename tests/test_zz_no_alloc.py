@@ -91,11 +91,12 @@ def test_noalloc_takes_no_device_memory(ra):
 
 
 def test_noalloc_accepts_exactly_its_scratch_size(ra):
-    # fp16 copy of V: 1 * 131072 * 1 * 128 * 2 bytes = 32 MiB exactly
+    # fp16 copy of V: 1 * 131072 * 1 * 128 * 2 bytes = 32 MiB exactly, plus
+    # the 256-byte unit counter
     N, scale = 131072, 128 ** -0.5
     from blockwise_exact_attention_ra_gb300.inputs import make_tensors
     q, k, v, _ = make_tensors(1, N, 1, 1, 128, torch.bfloat16, "cuda", 504, with_do=False)
-    assert ra.ra_ring_fwd_workspace_bytes(ra.RA_BF16, ra.shape_of(q, k), 32) == LIMIT
+    assert ra.ra_ring_fwd_workspace_bytes(ra.RA_BF16, ra.shape_of(q, k), 32) == LIMIT + 256
     o, lse = _outputs(q)
     assert _call_noalloc(ra, q, k, v, 32, ra.RA_CAUSAL, scale, o, lse) == 0, ra.ra_last_error()
     ra.ra_sync_status()
