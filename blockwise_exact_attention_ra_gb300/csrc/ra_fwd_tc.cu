@@ -39,13 +39,15 @@
 // grows by more than 8 (log2 units), so P <= 2^8, well inside fp16.
 #include <math.h>
 
+#include <type_traits>
+
 #include "ra_device.cuh"
 
 namespace ra {
 namespace {
 
 constexpr int kThreads = 320;
-constexpr int kStages = 4;
+constexpr int kStages = 4;  // the MMA loop relies on K/V stage pairs (1, 2) and (3, 0)
 constexpr float kRescaleThreshold = 8.0f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kLog2e = 1.4426950408889634f;
@@ -460,22 +462,30 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
         mma_commit(bar_kv_empty(sk));
         ++L_cnt;
         bool first_pv[2] = {a.mode == 0, a.mode == 0};
-        for (int it = it0, nx; it < ui.n_iter; it = nx) {
-          nx = VARLEN ? next_valid(ui, it, a) : it + 1;
-          const uint32_t sv = L_cnt % kStages;
-          if (!mbar_wait(bar_kv_full(sv), (L_cnt / kStages) & 1, abort_flag, a.status, lim)) { ok = false; break; }
+        // A unit takes an even number of K/V loads (its first K, then V(it)
+        // and K(it+1) per iteration, V alone at the last), so V(it) sits in
+        // stage 1 or 3 and K(it+1) in the stage after it, alternating from one
+        // iteration to the next.  Each iteration is built for its stage pair,
+        // which makes the descriptors and barrier addresses constants: with
+        // stage numbers computed at run time the descriptor arithmetic held the
+        // issue of each MMA above the tensor pipe's 64 cycles.
+        static_assert(kStages == 4, "stage pairs (1, 2) and (3, 0)");
+        int it = it0;
+        auto step = [&](auto sv_c) {  // false once the unit is done or a wait gave up
+          constexpr uint32_t sv = decltype(sv_c)::value, sk2 = (sv + 1) % kStages;
+          const int nx = VARLEN ? next_valid(ui, it, a) : it + 1;
+          if (!mbar_wait(bar_kv_full(sv), (L_cnt / kStages) & 1, abort_flag, a.status, lim)) return ok = false;
           ++L_cnt;
           const bool has_next = nx < ui.n_iter;
-          uint32_t sk2 = 0;
           if (has_next) {
-            sk2 = L_cnt % kStages;
-            if (!mbar_wait(bar_kv_full(sk2), (L_cnt / kStages) & 1, abort_flag, a.status, lim)) { ok = false; break; }
+            if (!mbar_wait(bar_kv_full(sk2), (L_cnt / kStages) & 1, abort_flag, a.status, lim)) return ok = false;
             ++L_cnt;
           }
           tc_fence_after();
-          for (int x = 0; x < 2 && ok; ++x) {
+#pragma unroll
+          for (int x = 0; x < 2; ++x) {
             if (active(ui, x, it)) {
-              if (!mbar_wait(bar_p_full(x), p_cnt[x] & 1, abort_flag, a.status, lim)) { ok = false; break; }
+              if (!mbar_wait(bar_p_full(x), p_cnt[x] & 1, abort_flag, a.status, lim)) return ok = false;
               ++p_cnt[x];
               tc_fence_after();
               issue_pv(x, sv, !first_pv[x]);
@@ -484,9 +494,16 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
             }
             if (has_next && active(ui, x, nx)) issue_s(x, sk2);
           }
-          if (!ok) break;
           mma_commit(bar_kv_empty(sv));
           if (has_next) mma_commit(bar_kv_empty(sk2));
+          it = nx;
+          return it < ui.n_iter;
+        };
+        bool more = it < ui.n_iter;
+        if (more && L_cnt % kStages == 3) more = step(std::integral_constant<uint32_t, 3>{});
+        while (more) {
+          more = step(std::integral_constant<uint32_t, 1>{});
+          if (more) more = step(std::integral_constant<uint32_t, 3>{});
         }
         if (!ok) break;
         mma_commit(BAR_Q_EMPTY);
