@@ -161,7 +161,7 @@ __device__ __forceinline__ int last_visible_tile(const TcFwdArgs& a, long long q
 // lightest units end the launch.
 // VARLEN selects the kernel built for variable host lengths; the other
 // builds see no length array and compile its checks away.
-template <bool VARLEN>
+template <bool VARLEN, bool STRIPED>
 __device__ __forceinline__ UnitInfo unit_info(const TcFwdArgs& a, int u) {
   UnitInfo r;
   int per_head;
@@ -179,7 +179,7 @@ __device__ __forceinline__ UnitInfo unit_info(const TcFwdArgs& a, int u) {
   const int nkt = (a.Nkv + 127) / 128;
   r.nkt = nkt;
   r.striped = 0;
-  if (a.ring_P > 0 && a.striped) {
+  if (STRIPED) {
     // striped: the row of a host's local row l holds position l * P + host; every
     // host has the same work, heaviest local pairs first
     const int T = a.ring_S / 128;
@@ -270,7 +270,7 @@ __device__ __forceinline__ UnitInfo unit_info(const TcFwdArgs& a, int u) {
   return r;
 }
 
-template <int D, bool PRECISE, bool VARLEN>
+template <int D, bool PRECISE, bool VARLEN, bool STRIPED>
 __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_constant__ TcFwdArgs a) {
   using L = FwdSmem<D>;
   extern __shared__ uint8_t smem_raw[];
@@ -363,7 +363,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
         unit_ring[slot] = u;
         mbar_arrive(bar_unit_full(slot));
         if (u >= a.num_units) break;
-        const UnitInfo ui = unit_info<VARLEN>(a, u);
+        const UnitInfo ui = unit_info<VARLEN, STRIPED>(a, u);
         if (ui.n_iter == 0) continue;  // no key of this block is visible to the unit
         if (!mbar_wait(BAR_Q_EMPTY, (k & 1) ^ 1, abort_flag, a.status, lim)) { ok = false; break; }
         ++k;
@@ -447,7 +447,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
       for (int n = 0; ok; ++n) {
         int u;
         if (!take_unit(n, &u) || u >= a.num_units) break;
-        const UnitInfo ui = unit_info<VARLEN>(a, u);
+        const UnitInfo ui = unit_info<VARLEN, STRIPED>(a, u);
         if (ui.n_iter == 0) continue;
         if (!mbar_wait(BAR_Q_FULL, k & 1, abort_flag, a.status, lim)) { ok = false; break; }
         ++k;
@@ -526,28 +526,29 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
     for (int n = 0; ok; ++n) {
       int u;
       if (!take_unit(n, &u) || u >= a.num_units) break;
-      const UnitInfo ui = unit_info<VARLEN>(a, u);
+      const UnitInfo ui = unit_info<VARLEN, STRIPED>(a, u);
       if ((VARLEN && ui.n_iter == 0) || !ever_active(ui, x)) continue;  // this tile sees no key in this unit
       const int row = ui.qa_row0 + x * 128 + r;  // tensor row
       // with variable host lengths, rows past their host's valid length are padding
       const bool row_ok = row < a.Nq && (!VARLEN || row % a.ring_S < host_len_at(a.host_len, row / a.ring_S, a.ring_S));
       const long long qpos = ui.qpos0[x] + r;
       float m_run = -INFINITY, l_run = 0.f;
-      const long long sidx = ((long long)ui.b * a.Hq + ui.h) * a.Nq + row;
-      const long long oidx = (((long long)ui.b * a.Nq + row) * a.Hq + ui.h) * D;
+      // row offsets of the state (m, l: [B, Hq, N]; o: [B, N, Hq, D]), formed where used
+      auto sidx = [&]() { return ((long long)ui.b * a.Hq + ui.h) * a.Nq + row; };
+      auto oidx = [&]() { return (((long long)ui.b * a.Nq + row) * a.Hq + ui.h) * D; };
       if (a.mode == 1) {
         // load the running state into registers and TMEM
         if (row_ok) {
-          const float mm = a.m_acc[sidx];
+          const float mm = a.m_acc[sidx()];
           m_run = mm == -INFINITY ? -INFINITY : mm * kLog2e;
-          l_run = a.l_acc[sidx];
+          l_run = a.l_acc[sidx()];
         }
 #pragma unroll
         for (int c = 0; c < D; c += 32) {
           uint32_t v[32];
 #pragma unroll
           for (int j = 0; j < 32; j += 4) {
-            float4 f = row_ok ? *reinterpret_cast<const float4*>(a.o_acc + oidx + c + j)
+            float4 f = row_ok ? *reinterpret_cast<const float4*>(a.o_acc + oidx() + c + j)
                               : make_float4(0.f, 0.f, 0.f, 0.f);
             v[j] = __float_as_uint(f.x);
             v[j + 1] = __float_as_uint(f.y);
@@ -694,7 +695,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
             }
           }
         }
-        if (row_ok) a.lse[sidx] = l_run > 0.f ? (m_run + log2f(l_run)) * kLn2 : -INFINITY;
+        if (row_ok) a.lse[sidx()] = l_run > 0.f ? (m_run + log2f(l_run)) * kLn2 : -INFINITY;
       } else {
 #pragma unroll
         for (int c = 0; c < D; c += 32) {
@@ -704,14 +705,14 @@ __global__ void __launch_bounds__(kThreads, 1) tc_fwd_kernel(const __grid_consta
           if (row_ok) {
 #pragma unroll
             for (int j = 0; j < 32; j += 4)
-              *reinterpret_cast<float4*>(a.o_acc + oidx + c + j) =
+              *reinterpret_cast<float4*>(a.o_acc + oidx() + c + j) =
                   make_float4(__uint_as_float(ov[j]), __uint_as_float(ov[j + 1]),
                               __uint_as_float(ov[j + 2]), __uint_as_float(ov[j + 3]));
           }
         }
         if (row_ok) {
-          a.m_acc[sidx] = m_run == -INFINITY ? -INFINITY : m_run * kLn2;
-          a.l_acc[sidx] = l_run;
+          a.m_acc[sidx()] = m_run == -INFINITY ? -INFINITY : m_run * kLn2;
+          a.l_acc[sidx()] = l_run;
         }
       }
       tc_fence_before();
@@ -736,16 +737,22 @@ cudaError_t launch_tc_fwd(TcFwdArgs& a, int num_sms, cudaStream_t st) {
     kernel<<<grid, kThreads, smem, st>>>(a);
     return cudaSuccess;
   };
+  // variable host lengths and the striped layout never come together (the
+  // entry points reject the pair)
+  auto pick = [&](auto d_c) {
+    constexpr int DD = decltype(d_c)::value;
+    constexpr int smem = FwdSmem<DD>::kAlloc;
+    const bool striped = a.ring_P > 0 && a.striped;
+    if (a.host_len)
+      return a.precise ? run(tc_fwd_kernel<DD, true, true, false>, smem) : run(tc_fwd_kernel<DD, false, true, false>, smem);
+    if (striped)
+      return a.precise ? run(tc_fwd_kernel<DD, true, false, true>, smem) : run(tc_fwd_kernel<DD, false, false, true>, smem);
+    return a.precise ? run(tc_fwd_kernel<DD, true, false, false>, smem) : run(tc_fwd_kernel<DD, false, false, false>, smem);
+  };
   if (a.d == 128)
-    e = a.host_len ? (a.precise ? run(tc_fwd_kernel<128, true, true>, FwdSmem<128>::kAlloc)
-                                : run(tc_fwd_kernel<128, false, true>, FwdSmem<128>::kAlloc))
-                   : (a.precise ? run(tc_fwd_kernel<128, true, false>, FwdSmem<128>::kAlloc)
-                                : run(tc_fwd_kernel<128, false, false>, FwdSmem<128>::kAlloc));
+    e = pick(std::integral_constant<int, 128>{});
   else if (a.d == 64)
-    e = a.host_len ? (a.precise ? run(tc_fwd_kernel<64, true, true>, FwdSmem<64>::kAlloc)
-                               : run(tc_fwd_kernel<64, false, true>, FwdSmem<64>::kAlloc))
-                   : (a.precise ? run(tc_fwd_kernel<64, true, false>, FwdSmem<64>::kAlloc)
-                                : run(tc_fwd_kernel<64, false, false>, FwdSmem<64>::kAlloc));
+    e = pick(std::integral_constant<int, 64>{});
   else
     return cudaErrorInvalidValue;
   if (e != cudaSuccess) return e;
