@@ -93,6 +93,26 @@ def test_tc_ring_softmax_stress(ra):
 
 
 @pytest.mark.parametrize("causal", [True, False])
+def test_tc_fwd_maximum_rising_within_a_tile(ra, causal):
+    # Keys 64-127 of every 128-key tile are scaled by 8 (exact in bf16), so their
+    # scores spread ~8x wider than those of keys 0-63: in the first tile a row
+    # meets, the second half of the keys raises the maximum by ~20 log2 units
+    # after the first half's exponentials were taken, far past the rescale
+    # threshold.  The default numerics handle a tile in two halves of 64 keys and
+    # rescale the first half's P and sum then; O and LSE must still match.
+    q, k, v, _ = _inputs(1, 1024, 2, 2, 128, torch.bfloat16, 41)
+    upper = (torch.arange(1024, device=k.device) % 128) >= 64
+    k = k.clone()
+    k[:, upper] *= 8
+    scale = 128 ** -0.5
+    o, lse = ra.ring_attention_fwd(q, k, v, 4, causal, scale)
+    ra.ra_sync_status()
+    rO, rL = oracle.attention_fwd(f64(q), f64(k), f64(v), causal, scale)
+    check("O", f64(o), rO, torch.bfloat16)
+    check("LSE", f64(lse), rL, torch.bfloat16, kind="lse")
+
+
+@pytest.mark.parametrize("causal", [True, False])
 def test_tc_ring_precise_mode_on_plain_inputs(ra, causal):
     _ring_case(ra, 2, 1024, 4, 2, 128, 4, causal, torch.bfloat16, 38, precise=True)
 
