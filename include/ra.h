@@ -37,7 +37,11 @@
  * Streams.  `stream` is a cudaStream_t passed as void* (NULL = legacy default
  *   stream).  Every call only enqueues work and returns; it holds no pointer
  *   after it returns and allocates no device memory: the caller owns every
- *   buffer, including the workspace.
+ *   buffer, including the workspace.  A call's work (kernels and the
+ *   cudaMemsetAsync that zeroes its workspace's counters and accumulators)
+ *   all goes to `stream`, so calls can be captured into a CUDA graph and
+ *   replayed, provided one call has run on the device beforehand (the first
+ *   call looks up the library's device status word).
  * Errors.  The return value reports argument validation and launch errors
  *   (ra_status).  Errors found on the device (a value out of fp16 range in a
  *   bf16 -> fp16 operand copy, a bounded wait that ran out) are recorded in a
