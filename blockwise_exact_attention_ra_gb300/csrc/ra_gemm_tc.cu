@@ -51,17 +51,27 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
 // whose e^{-x^2} = e^{-u^2/2} is also the exponential of phi(u).  One
 // exponential and one reciprocal per element, against an erf and an exp;
 // the error is far below the 16-bit rounding of the outputs.
-__device__ __forceinline__ float gelu_f(float u, float* grad) {
-  const float x = fabsf(u) * 0.70710678118654752f;
-  float t;
-  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(t) : "f"(fmaf(0.3275911f, x, 1.f)));
-  const float e = ex2_approx(-0.72134752044448170f * (u * u));  // e^{-u^2/2} = 2^{-u^2 log2(e) / 2}
-  const float poly =
-      t * fmaf(t, fmaf(t, fmaf(t, fmaf(t, 1.061405429f, -1.453152027f), 1.421413741f), -0.284496736f),
-               0.254829592f);
-  const float cdf = 0.5f + copysignf(0.5f - 0.5f * poly * e, u);  // (1 + sign(u) erf(|u| / sqrt 2)) / 2
-  if (grad) *grad = cdf + u * 0.39894228040143268f * e;
-  return u * cdf;
+template <bool GRAD>
+__device__ __forceinline__ void gelu2_f(float2 u, float2* out, float2* grad) {
+  // two elements at a time with the packed fp32x2 operations (FMA pipe)
+  const float2 x = make_float2(fabsf(u.x) * 0.70710678118654752f, fabsf(u.y) * 0.70710678118654752f);
+  const float2 d = __ffma2_rn(make_float2(0.3275911f, 0.3275911f), x, make_float2(1.f, 1.f));
+  float2 t;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(t.x) : "f"(d.x));
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(t.y) : "f"(d.y));
+  const float2 uu = __fmul2_rn(u, u);
+  // e^{-u^2/2} = 2^{-u^2 log2(e) / 2}
+  const float2 e = make_float2(ex2_approx(-0.72134752044448170f * uu.x), ex2_approx(-0.72134752044448170f * uu.y));
+  float2 p = __ffma2_rn(t, make_float2(1.061405429f, 1.061405429f), make_float2(-1.453152027f, -1.453152027f));
+  p = __ffma2_rn(t, p, make_float2(1.421413741f, 1.421413741f));
+  p = __ffma2_rn(t, p, make_float2(-0.284496736f, -0.284496736f));
+  p = __ffma2_rn(t, p, make_float2(0.254829592f, 0.254829592f));
+  p = __fmul2_rn(t, p);
+  // (1 - poly e) / 2 = erf(|u| / sqrt 2) / 2
+  const float2 h = __ffma2_rn(make_float2(-0.5f, -0.5f), __fmul2_rn(p, e), make_float2(0.5f, 0.5f));
+  const float2 cdf = make_float2(0.5f + copysignf(h.x, u.x), 0.5f + copysignf(h.y, u.y));
+  *out = __fmul2_rn(u, cdf);
+  if (GRAD) *grad = __ffma2_rn(__fmul2_rn(u, make_float2(0.39894228040143268f, 0.39894228040143268f)), e, cdf);
 }
 
 __device__ __forceinline__ uint32_t pack16(float lo, float hi, int bf16) {
@@ -268,12 +278,24 @@ __global__ void __launch_bounds__(kThreads, 1) tc_gemm_kernel(const __grid_const
           }
         } else if (EPI == GEMM_GELU) {
 #pragma unroll
-          for (int j = 0; j < 32; ++j) v[j] = gelu_f(v[j], nullptr);
+          for (int j = 0; j < 32; j += 2) {
+            float2 o;
+            gelu2_f<false>(make_float2(v[j], v[j + 1]), &o, nullptr);
+            v[j] = o.x;
+            v[j + 1] = o.y;
+          }
           store16x32(static_cast<uint16_t*>(cbase) + off, v, bf16);
         } else if (EPI == GEMM_GELU2) {
           float g[32];
 #pragma unroll
-          for (int j = 0; j < 32; ++j) v[j] = gelu_f(v[j], &g[j]);
+          for (int j = 0; j < 32; j += 2) {
+            float2 o, gr;
+            gelu2_f<true>(make_float2(v[j], v[j + 1]), &o, &gr);
+            v[j] = o.x;
+            v[j + 1] = o.y;
+            g[j] = gr.x;
+            g[j + 1] = gr.y;
+          }
           store16x32(static_cast<uint16_t*>(cbase) + off, v, bf16);
           store16x32(static_cast<uint16_t*>(a.c2) + off, g, bf16);
         } else if (EPI == GEMM_MUL) {
