@@ -206,7 +206,13 @@ size_t ra_ring_fwd_workspace_bytes(ra_dtype dtype, ra_shape shape, int P);
  *   dS_ij = P_ij (dO_i . v_j - D_i); dQ_i = scale sum_j dS_ij k_j;
  *   dK_j = scale sum_i dS_ij q_i (summed over the query heads of a group).
  *   o in o_dtype, dO in dtype, lse from ra_ring_fwd; dq [B,N,Hq,d],
- *   dk, dv [B,N,Hkv,d] written in grad_dtype (fully overwritten). */
+ *   dk, dv [B,N,Hkv,d] written in grad_dtype (fully overwritten).
+ *   workspace: device memory, 256-byte aligned, at least
+ *   ra_ring_bwd_workspace_bytes() bytes: D and LSE*log2(e) per row, for
+ *   16-bit dtypes the fp32 dQ accumulator and the counter the kernel's CTAs
+ *   draw their work from (both zeroed by each call), and for bf16 the fp16
+ *   copies of q, k, v, dO.  It must not be in use by work that overlaps the
+ *   call on the GPU. */
 int ra_ring_bwd(const void* q, const void* k, const void* v, const void* o,
                 ra_dtype o_dtype, const void* dO, const float* lse,
                 ra_dtype dtype, ra_shape shape, int P, int flags, float scale,
