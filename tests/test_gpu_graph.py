@@ -1,4 +1,5 @@
-"""The ring forward and backward captured into a CUDA graph and replayed.
+"""The ring forward and backward captured into a CUDA graph and replayed, and
+the workspace the forward needs for its work counter.
 
 Every launch of a call goes to the caller's stream and the workspaces are the
 caller's, so a training step can be captured once and replayed; that includes
@@ -64,3 +65,26 @@ def test_ring_step_replays_from_a_cuda_graph(ra, striped):
             assert torch.equal(got, want), name
         err = (dq - ref[2]).abs().max().item()
         assert err <= 1e-5 * ref[2].abs().max().item(), f"dQ differs by {err}"
+
+
+@pytest.mark.parametrize("dtype", [torch.float16, torch.bfloat16])
+def test_ring_fwd_refuses_a_workspace_without_room_for_its_counter(ra, dtype):
+    # the 16-bit forward draws its work from a counter in the workspace, fp16
+    # inputs included: a missing or short workspace is refused before any launch
+    import ctypes
+    from blockwise_exact_attention_ra_gb300.inputs import make_tensors
+    q, k, v, _ = make_tensors(1, 512, 2, 2, 128, dtype, "cuda", 78, with_do=False)
+    sh = ra.shape_of(q, k)
+    need = ra.ra_ring_fwd_workspace_bytes(ra._dt(q), sh, 2)
+    assert need >= 256
+    o = torch.empty(1, 512, 2, 128, device="cuda")
+    lse = torch.empty(1, 2, 512, device="cuda")
+    vp = ctypes.c_void_p
+    args = [vp(q.data_ptr()), vp(k.data_ptr()), vp(v.data_ptr()), ra._dt(q), sh, 2, 1, ctypes.c_float(0.1),
+            vp(o.data_ptr()), ra.RA_F32, vp(lse.data_ptr())]
+    assert ra.lib.ra_ring_fwd(*args, None, 0, None) == 1
+    assert "workspace" in ra.ra_last_error()
+    ws = torch.empty(need, dtype=torch.uint8, device="cuda")
+    assert ra.lib.ra_ring_fwd(*args, vp(ws.data_ptr()), need - 1, None) == 1
+    assert ra.lib.ra_ring_fwd(*args, vp(ws.data_ptr()), need, None) == 0, ra.ra_last_error()
+    ra.ra_sync_status()
